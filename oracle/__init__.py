@@ -1,0 +1,115 @@
+"""The oracle: a plain fp64 CPU statement of the fused gate-up SwiGLU.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``gate_up_swiglu_gb300``) never imports it and shares no code with
+it.
+
+``swiglu_oracle.c`` holds the arithmetic (cited there); this module compiles it
+with gcc into ``oracle/_build/liboracle_swiglu.so`` and marshals torch CPU
+tensors to it.  Parity status: forward and both backward variants are pinned by
+``tests/test_oracle.py`` (closed forms, the Lambert-W stationary point,
+finite differences, torch float64 autograd on the two-tensor formulation,
+brute-force rounding checks and planted-mistake tests).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swiglu_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle_swiglu.so")
+
+F32, BF16, F64 = 0, 1, 2
+_CODE = {torch.float32: F32, torch.bfloat16: BF16, torch.float64: F64}
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_library(src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle C source into a shared library; return its path."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp%d" % os.getpid()
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_library()
+    return _LIB
+
+
+def load(path: str = None):
+    """Load (building first if needed) the oracle library and declare its calls."""
+    global _lib
+    with _lock:
+        if path is None and _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(path or build())
+        i64, vp = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_swiglu_fwd.argtypes = [vp, vp, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_swiglu_fwd.restype = ctypes.c_int
+        lib.oracle_swiglu_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_swiglu_bwd.restype = ctypes.c_int
+        lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_from_double.restype = ctypes.c_uint16
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _rowmajor(t: torch.Tensor, name: str) -> None:
+    if t.device.type != "cpu":
+        raise ValueError(f"oracle: {name} must be a CPU tensor")
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"oracle: {name} must be 2D with unit column stride")
+
+
+def fwd(x: torch.Tensor, y: torch.Tensor = None, lib=None) -> torch.Tensor:
+    """y[r, j] = silu(x[r, j]) * x[r, n + j], rounded once to x's dtype."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    rows, two_n = x.shape
+    n = two_n // 2
+    if y is None:
+        y = torch.empty((rows, n), dtype=x.dtype)
+    _rowmajor(y, "y")
+    rc = lib.oracle_swiglu_fwd(x.data_ptr(), y.data_ptr(), rows, n, x.stride(0), y.stride(0),
+                               _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_fwd rejected its arguments")
+    return y
+
+
+def bwd(dy: torch.Tensor, x: torch.Tensor, dx: torch.Tensor = None, lib=None) -> torch.Tensor:
+    """dx[:, :n] = d(gate), dx[:, n:] = d(up); pass dx=x for the in-place form."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    _rowmajor(dy, "dy")
+    rows, two_n = x.shape
+    n = two_n // 2
+    if dx is None:
+        dx = torch.empty((rows, 2 * n), dtype=x.dtype)
+    _rowmajor(dx, "dx")
+    rc = lib.oracle_swiglu_bwd(dy.data_ptr(), x.data_ptr(), dx.data_ptr(), rows, n, dy.stride(0),
+                               x.stride(0), dx.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_bwd rejected its arguments")
+    return dx
+
+
+def bf16_from_double(v: float, lib=None) -> int:
+    """Bits of the bf16 nearest to ``v`` (ties to even)."""
+    lib = lib or load()
+    return int(lib.oracle_bf16_from_double(float(v)))

@@ -1,0 +1,163 @@
+/*
+ * oracle/swiglu_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU statement of what the fused gate-up
+ * SwiGLU computes.  It exists to check the CUDA library against; nothing in the
+ * product path may link or call it (only the tests, the smoke check and the
+ * bench's CPU-baseline leg do).  It shares no code, header or constant with the
+ * CUDA side.
+ *
+ * Source of each step (Liger-Kernel Megatron SwiGLU page):
+ *   - layout, §Background: Megatron's linear_fc1 emits one [tokens, 2n] buffer,
+ *     gate in columns [0, n), up in [n, 2n); the fused kernel reads both halves
+ *     through a column offset, input row stride 2n, output row stride n.
+ *   - activation, §Summary / §Background: SwiGLU as Megatron's bias_swiglu_impl
+ *     computes it with bias=None, y = silu(gate) * up, silu(g) = g * sigmoid(g).
+ *   - backward, §What's added / §Optional in_place: the backward works from the
+ *     saved fc1 buffer (recomputing sigmoid) and writes d(gate) into [0, n) and
+ *     d(up) into [n, 2n).  The page prints no formula; the one used is the
+ *     analytic derivative of silu(g) * u:
+ *        d(gate) = dy * u * s * (1 + g * (1 - s)),   d(up) = dy * g * s,
+ *     with s = 1 / (1 + exp(-g)).
+ *
+ * Arithmetic: every input is widened exactly to double (bf16 -> fp32 -> double
+ * are exact), the formulas above are evaluated in double with libm exp, and each
+ * result is rounded once to the storage type, round-to-nearest-even.  The bf16
+ * rounding is done directly from the double (no intermediate fp32 rounding).
+ * No blocking, fusion or reordering: one loop over rows, one over columns.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, no
+ * FMA contraction, so x86 and Arm hosts give the same bits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+#define ORACLE_F64 2
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG -1
+
+/* ---- storage types ------------------------------------------------------ */
+
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16; /* bf16 is the top half of an fp32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 (8 exponent bits, 8 significand bits
+ * including the hidden one), ties to even, in one step.  The spacing of bf16
+ * numbers in [2^k, 2^(k+1)) is 2^(k-7) for k >= -126, and 2^-133 in the
+ * subnormal range below 2^-126. */
+uint16_t oracle_bf16_from_double(double v) {
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e); /* a in [2^(e-1), 2^e) */
+    int k = e - 1;
+    if (k < -126) k = -126;
+    double spacing = ldexp(1.0, k - 7);
+    double q = nearbyint(a / spacing); /* a / spacing is exact; ties to even */
+    double r = q * spacing;
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u); /* overflow */
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+static double load_elem(const void *base, int64_t idx, int dtype) {
+    const char *p = (const char *)base;
+    if (dtype == ORACLE_F32) {
+        float f;
+        memcpy(&f, p + idx * 4, 4);
+        return (double)f;
+    }
+    if (dtype == ORACLE_BF16) {
+        uint16_t h;
+        memcpy(&h, p + idx * 2, 2);
+        return bf16_bits_to_double(h);
+    }
+    double d;
+    memcpy(&d, p + idx * 8, 8);
+    return d;
+}
+
+static void store_elem(void *base, int64_t idx, int dtype, double v) {
+    char *p = (char *)base;
+    if (dtype == ORACLE_F32) {
+        float f = (float)v; /* IEEE conversion, round to nearest even */
+        memcpy(p + idx * 4, &f, 4);
+    } else if (dtype == ORACLE_BF16) {
+        uint16_t h = oracle_bf16_from_double(v);
+        memcpy(p + idx * 2, &h, 2);
+    } else {
+        memcpy(p + idx * 8, &v, 8);
+    }
+}
+
+/* ---- the method, one element pair at a time ------------------------------ */
+
+static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+/* forward: y = silu(g) * u = g * s * u */
+static double swiglu_fwd_pair(double g, double u) {
+    double s = sigmoid(g);
+    return g * s * u;
+}
+
+/* backward: the derivative of g * s(g) * u with respect to g and to u, times dy */
+static void swiglu_bwd_pair(double dy, double g, double u, double *dgate, double *dup) {
+    double s = sigmoid(g);
+    *dgate = dy * u * s * (1.0 + g * (1.0 - s));
+    *dup = dy * g * s;
+}
+
+/* ---- the layouts ----------------------------------------------------------- */
+
+static int check_args(int64_t rows, int64_t n, int dtype) {
+    if (rows < 0 || n < 0) return ORACLE_BAD_ARG;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return ORACLE_BAD_ARG;
+    return ORACLE_OK;
+}
+
+/* x: [rows, 2n] with row stride sx (elements); y: [rows, n] with row stride sy. */
+int oracle_swiglu_fwd(const void *x, void *y, int64_t rows, int64_t n, int64_t sx, int64_t sy,
+                      int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double g = load_elem(x, r * sx + j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype);
+            store_elem(y, r * sy + j, dtype, swiglu_fwd_pair(g, u));
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* dy: [rows, n] (stride sdy); x: [rows, 2n] (stride sx); dx: [rows, 2n] (stride
+ * sdx) receives d(gate) in [0, n) and d(up) in [n, 2n).  dx may be x itself (the
+ * in-place backward): each pair is read before it is written. */
+int oracle_swiglu_bwd(const void *dy, const void *x, void *dx, int64_t rows, int64_t n,
+                      int64_t sdy, int64_t sx, int64_t sdx, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double d = load_elem(dy, r * sdy + j, dtype);
+            double g = load_elem(x, r * sx + j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype);
+            double dg, du;
+            swiglu_bwd_pair(d, g, u, &dg, &du);
+            store_elem(dx, r * sdx + j, dtype, dg);
+            store_elem(dx, r * sdx + n + j, dtype, du);
+        }
+    }
+    return ORACLE_OK;
+}
