@@ -1,0 +1,436 @@
+"""Bench of the fused gate-up SwiGLU on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+One step = one forward plus one out-of-place backward (the "fwd+bwd" of the
+Liger-Kernel Megatron SwiGLU page, §Summary) over the large-FFN bf16 workload
+x [S=2048, B=4, 2n=65536] (ffn_local = 32768; 1 GiB input, larger than L2, so
+no L2 flush is needed between steps).  Inputs are seeded synthetic tensors
+(workloads.py) already resident in HBM when the timed region starts.  Prints
+ONE JSON line on rank 0.
+
+The value is milliseconds per step (lower is better).  Alongside: forward-
+and backward-only times, in-place backward time, achieved HBM GB/s against the
+measured copy bandwidth, an end-to-end time through host buffers, and the
+oracle timed on the host's cores on a bounded sample of the same workload.
+
+Under torchrun (--gpus N > 1) every rank runs the whole workload on its own GPU
+(independent replicas: the op has no exchange step), time is the max over
+ranks, and the line reports "scaling": "weak".
+
+--impl reference times the oracle (the plain fp64 CPU statement of the op) on
+the host's cores instead, each step a bounded row sample of the same workload
+scaled to the full workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "SwiGLU gate-up fwd & fwd+bwd ms, HBM GB/s, % of GB300 peak (bf16 S2048 B4)"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "gate_up_swiglu_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------ setup ---
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    """Digest of the kernel sources, to tell whether stored ncu counters still
+    describe the current kernels."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key: str, workload: str):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+    except (OSError, KeyError, ValueError):
+        return None
+    if e.get("source_digest") != source_digest() or e.get("workload") != workload:
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        sel = str(device_index)
+        try:
+            uuid = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+            if uuid is not None:
+                s = str(uuid)
+                sel = s if s.startswith("GPU-") else "GPU-" + s
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5 and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:  # timed region shorter than the sampling period
+            inside = [p for t, p in self.samples if t <= t1][-3:]
+            window = "warmup+timed"
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        smax = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def time_oracle(w: W.Workload, target_s: float):
+    """Time the oracle's forward + backward on a row sample sized to about
+    `target_s` seconds; return (ms per full-workload step, rows sampled, seconds)."""
+    import oracle  # the oracle is only ever timed here, never used for results
+
+    lib = oracle.load()
+
+    def run(rows):
+        x, dy = W.make_inputs(w, "cpu", rows=rows)
+        t = time.perf_counter()
+        oracle.fwd(x, lib=lib)
+        oracle.bwd(dy, x, lib=lib)
+        return time.perf_counter() - t
+
+    rows = 8
+    dt = run(rows)
+    per_row = dt / rows
+    rows = int(max(8, min(w.rows, target_s / max(per_row, 1e-9))))
+    dt = run(rows)
+    return dt / rows * w.rows * 1e3, rows, dt
+
+
+# ------------------------------------------------------------------ arms ---
+
+def reference_arm(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = max(0.05, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    import oracle
+
+    lib = oracle.load()
+    x, dy = W.make_inputs(w, "cpu", rows=max(1, min(w.rows, 64)))
+    t = time.perf_counter()
+    oracle.fwd(x, lib=lib)
+    oracle.bwd(dy, x, lib=lib)
+    per_row = (time.perf_counter() - t) / x.shape[0]
+    rows = int(max(1, min(w.rows, per_step / max(per_row, 1e-9))))
+    x, dy = W.make_inputs(w, "cpu", rows=rows)
+    for _ in range(args.warmup):
+        oracle.fwd(x, lib=lib)
+        oracle.bwd(dy, x, lib=lib)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.fwd(x, lib=lib)
+        oracle.bwd(dy, x, lib=lib)
+        times.append(time.perf_counter() - t)
+    ms = statistics.mean(times) / rows * w.rows * 1e3
+    sample = f"{rows} of {w.rows} rows per step, scaled to the full workload; single thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": list(w.shape), "ffn_local": w.n,
+                   "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd"},
+        "cpu_baseline": {"value": round(ms, 3), "unit": "ms", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, w):
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libswiglu has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl", device_id=dev)
+        pg = dist
+
+    from gate_up_swiglu_gb300 import build
+
+    build.build()
+    import gate_up_swiglu_gb300 as sw
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if pg is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    x, dy = W.make_inputs(w, dev)
+    x = x.contiguous()
+    y = torch.empty((w.rows, w.n), dtype=x.dtype, device=dev)
+    dx = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    lib = sw.lib
+    dt_code = sw.SWIGLU_BF16 if w.dtype == W.BF16 else sw.SWIGLU_F32
+    rows, n = w.rows, w.n
+
+    def fwd():
+        st = lib.swiglu_gateup_fwd(x.data_ptr(), y.data_ptr(), rows, n, 2 * n, n, dt_code, sh)
+        if st:
+            raise sw.SwigluError(st, "fwd")
+
+    def bwd(out, in_place):
+        st = lib.swiglu_gateup_bwd(dy.data_ptr(), x.data_ptr(), out.data_ptr(), rows, n, n, 2 * n,
+                                   2 * n, dt_code, 1 if in_place else 0, sh)
+        if st:
+            raise sw.SwigluError(st, "bwd")
+
+    for _ in range(max(3, args.warmup)):
+        fwd()
+        bwd(dx, False)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for k in range(K):
+        ev[k][0].record(stream)
+        fwd()
+        ev[k][1].record(stream)
+        bwd(dx, False)
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    launches = 2 * K
+    fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    ms_step = max_over_ranks(total_ms / K)
+    fwd_avg = max_over_ranks(statistics.mean(fwd_ms))
+    bwd_avg = max_over_ranks(statistics.mean(bwd_ms))
+    clk = clocks.summary(t_wall0, t_wall1)
+    clocks.stop()
+
+    # in-place backward: x is restored from a copy between launches, outside
+    # the events, so each timed launch sees the forward input
+    x_saved = x.clone()
+    ip_ms = []
+    for k in range(min(K, 50)):
+        x.copy_(x_saved)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        bwd(x, True)
+        b.record(stream)
+        b.synchronize()
+        ip_ms.append(a.elapsed_time(b))
+    x.copy_(x_saved)
+    del x_saved
+    ip_avg = max_over_ranks(statistics.mean(ip_ms))
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(sw, w, x, dy, dev, K=min(K, 20), barrier=barrier, reduce=max_over_ranks)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        ms, srows, secs = time_oracle(w, target_s=args.cpu_seconds)
+        cpu = {"value": round(ms, 3), "unit": "ms", "cores": 1, "kind": "oracle",
+               "sample": f"{srows} of {w.rows} rows (fwd + bwd, {secs:.1f} s single thread), "
+                         "scaled to the full workload"}
+
+    if rank != 0:
+        return
+    peak, peak_src = measured_peaks()
+    fb, bb = w.fwd_bytes(), w.bwd_bytes()
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    bwd_gbs = gbs(bb, bwd_avg)
+    traffic = stored_traffic("bwd", w.name)
+    line = {
+        "metric": METRIC, "value": round(ms_step, 4), "unit": "ms", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "shape": list(w.shape), "ffn_local": n,
+                   "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "no flush: every step streams 4.3 GB, inputs 1.5 GiB > 129 MB L2"},
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
+        "bwd_in_place_ms": round(ip_avg, 4),
+        "fwd_gbs": round(gbs(fb, fwd_avg), 1), "bwd_gbs": round(bwd_gbs, 1),
+        "fwdbwd_gbs": round(gbs(fb + bb, fwd_avg + bwd_avg), 1),
+        "bwd_in_place_gbs": round(gbs(bb, ip_avg), 1),
+        "frac_of_measured_hbm": {"fwd": round(gbs(fb, fwd_avg) / peak, 4),
+                                 "fwdbwd": round(gbs(fb + bb, fwd_avg + bwd_avg) / peak, 4),
+                                 "peak_gbs": peak, "peak_source": peak_src},
+        "frac_of_8000_gbs": {"fwd": round(gbs(fb, fwd_avg) / 8000, 4),
+                             "fwdbwd": round(gbs(fb + bb, fwd_avg + bwd_avg) / 8000, 4)},
+        "roofline": {"bound": "hbm", "kernel": "swiglu_bwd_kernel (out of place)",
+                     "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(bwd_gbs / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic, "algorithmic_bytes": bb},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
+    """Same step through the public binding with the inputs copied in from pinned
+    host memory and the results copied back, all inside the timed region."""
+    xh = torch.empty(x_dev.shape, dtype=x_dev.dtype, pin_memory=True)
+    dyh = torch.empty(dy_dev.shape, dtype=dy_dev.dtype, pin_memory=True)
+    xh.copy_(x_dev)
+    dyh.copy_(dy_dev)
+    yh = torch.empty((w.rows, w.n), dtype=x_dev.dtype, pin_memory=True)
+    dxh = torch.empty(x_dev.shape, dtype=x_dev.dtype, pin_memory=True)
+    xd = torch.empty_like(x_dev)
+    dyd = torch.empty_like(dy_dev)
+    yd = torch.empty((w.rows, w.n), dtype=x_dev.dtype, device=dev)
+    dxd = torch.empty_like(x_dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        sw.swiglu_gateup_fwd(xd, yd, stream=stream)
+        sw.swiglu_gateup_bwd(dyd, xd, dxd, stream=stream)
+        yh.copy_(yd, non_blocking=True)
+        dxh.copy_(dxd, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = reduce(a.elapsed_time(b) / K)
+    h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
+    d2h = yh.numel() * yh.element_size() + dxh.numel() * dxh.element_size()
+    return {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        ours_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

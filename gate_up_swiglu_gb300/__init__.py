@@ -1,0 +1,158 @@
+"""Python binding of libswiglu, the GB300 fused gate-up SwiGLU.
+
+Argument marshalling only: every element of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/swiglu.h``.  There is no CPU or
+eager fallback: if ``libswiglu.so`` has not been built, importing this package
+raises.
+
+    y  = swiglu_gateup_fwd(x)                       # x: [..., 2n] CUDA tensor
+    dx = swiglu_gateup_bwd(dy, x)                   # new [..., 2n] gradient
+    swiglu_gateup_bwd(dy, x, in_place=True)         # gradient written over x
+
+``x`` is Megatron's ``linear_fc1`` output, gate in columns ``[0, n)`` and up in
+``[n, 2n)`` (Liger-Kernel Megatron SwiGLU page, §Background).  2D
+``[tokens, 2n]`` and 3D ``[s, b, 2n]`` tensors are flattened to rows without a
+copy (§Megatron feature compatibility).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libswiglu.so")
+
+SWIGLU_F32, SWIGLU_BF16 = 0, 1
+_DTYPE = {torch.float32: SWIGLU_F32, torch.bfloat16: SWIGLU_BF16}
+
+STATUS = {0: "SWIGLU_OK", -1: "SWIGLU_ERR_NULL", -2: "SWIGLU_ERR_DTYPE", -3: "SWIGLU_ERR_SHAPE",
+          -4: "SWIGLU_ERR_STRIDE", -5: "SWIGLU_ERR_ALIAS", -6: "SWIGLU_ERR_CUDA"}
+
+# every symbol include/swiglu.h declares
+EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_status_string",
+           "swiglu_last_cuda_error", "swiglu_abi_version")
+
+
+class SwigluError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libswiglu.so is not built ({LIB_PATH} missing); build it with "
+            "`python -m gate_up_swiglu_gb300.build` or __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.swiglu_gateup_fwd.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
+    lib.swiglu_gateup_fwd.restype = i32
+    lib.swiglu_gateup_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
+    lib.swiglu_gateup_bwd.restype = i32
+    lib.swiglu_status_string.argtypes = [i32]
+    lib.swiglu_status_string.restype = ctypes.c_char_p
+    lib.swiglu_last_cuda_error.argtypes = []
+    lib.swiglu_last_cuda_error.restype = i32
+    lib.swiglu_abi_version.argtypes = []
+    lib.swiglu_abi_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.swiglu_status_string(int(status)).decode()
+
+
+def _rows_view(t: torch.Tensor, name: str):
+    """(rows, cols, row_stride) of a [..., cols] tensor whose leading dims
+    flatten to evenly strided rows of unit-stride elements, without a copy."""
+    if t.dim() < 1:
+        raise ValueError(f"{name} must have at least one dimension")
+    cols = t.shape[-1]
+    if cols > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    lead = t.shape[:-1]
+    rows = 1
+    for d in lead:
+        rows *= d
+    if t.dim() == 1:
+        return 1, cols, cols
+    # the leading dims must collapse into one stride: stride[i] = stride[i+1] * shape[i+1]
+    stride = t.stride(-2)
+    for i in range(t.dim() - 3, -1, -1):
+        if t.shape[i] > 1 and t.stride(i) != t.stride(i + 1) * t.shape[i + 1]:
+            raise ValueError(f"{name}: leading dimensions do not flatten to evenly strided rows")
+    if rows <= 1:
+        stride = max(stride, cols)
+    return rows, cols, stride
+
+
+def _stream_handle(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("libswiglu operates on CUDA tensors only")
+    dev = ts[0].device
+    for t in ts[1:]:
+        if t.device != dev:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if ts[0].dtype not in _DTYPE or any(t.dtype != ts[0].dtype for t in ts):
+        raise ValueError("tensors must all be float32 or all bfloat16")
+
+
+def swiglu_gateup_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """y[..., j] = silu(x[..., j]) * x[..., n + j]; returns y ([..., n])."""
+    if y is None:
+        y = torch.empty((*x.shape[:-1], x.shape[-1] // 2), dtype=x.dtype, device=x.device)
+    _check_cuda(x, y)
+    if x.shape[-1] % 2:
+        raise ValueError("x's last dimension must be even (gate and up halves)")
+    rows, two_n, sx = _rows_view(x, "x")
+    yrows, n, sy = _rows_view(y, "y")
+    if yrows != rows or n * 2 != two_n:
+        raise ValueError("y must be [..., n] with the rows of x")
+    with torch.cuda.device(x.device):
+        st = lib.swiglu_gateup_fwd(x.data_ptr(), y.data_ptr(), rows, n, sx, sy, _DTYPE[x.dtype],
+                                   _stream_handle(x, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_fwd")
+    return y
+
+
+def swiglu_gateup_bwd(dy: torch.Tensor, x: torch.Tensor, dx: torch.Tensor = None,
+                      in_place: bool = False, stream=None) -> torch.Tensor:
+    """Gradient of silu(gate) * up w.r.t. x; d gate in [..., :n], d up in [..., n:].
+
+    ``in_place=True`` writes the gradient over ``x`` and returns ``x``."""
+    if in_place:
+        if dx is not None and dx.data_ptr() != x.data_ptr():
+            raise ValueError("in_place=True writes over x; dx must be None or x")
+        dx = x
+    elif dx is None:
+        dx = torch.empty_like(x, memory_format=torch.contiguous_format)
+    _check_cuda(dy, x, dx)
+    rows, two_n, sx = _rows_view(x, "x")
+    dyrows, n, sdy = _rows_view(dy, "dy")
+    dxrows, dxcols, sdx = _rows_view(dx, "dx")
+    if two_n % 2 or dyrows != rows or n * 2 != two_n or dxrows != rows or dxcols != two_n:
+        raise ValueError("shapes must be dy [..., n], x [..., 2n], dx [..., 2n] over the same rows")
+    with torch.cuda.device(x.device):
+        st = lib.swiglu_gateup_bwd(dy.data_ptr(), x.data_ptr(), dx.data_ptr(), rows, n, sdy, sx, sdx,
+                                   _DTYPE[x.dtype], 1 if in_place else 0, _stream_handle(x, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_bwd")
+    return dx
+
+
+__all__ = ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "status_string", "SwigluError", "lib",
+           "SWIGLU_F32", "SWIGLU_BF16", "EXPORTS", "LIB_PATH"]

@@ -1,0 +1,59 @@
+"""Compile libswiglu.so for sm_103a with nvcc, in-tree.
+
+    python -m gate_up_swiglu_gb300.build [--ptxas-info]
+
+The library is one translation unit (the C ABI plus the kernel templates it
+instantiates), linked against the static CUDA runtime so the .so depends on
+nothing but the driver.  No fast-math: the kernels choose every approximate
+operation explicitly and must keep subnormal results.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libswiglu.so")
+SOURCES = [os.path.join(CSRC, "swiglu_abi.cu")]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: libswiglu needs the CUDA toolkit to build")
+
+
+def command(out: str = LIB, ptxas_info: bool = False):
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+           "-shared", "-cudart", "static", "-I", INCLUDE, "-I", CSRC, "-o", out, *SOURCES]
+    if ptxas_info:
+        cmd.insert(1, "-Xptxas=-v")
+    return cmd
+
+
+def _stale(out: str) -> bool:
+    if not os.path.exists(out):
+        return True
+    t = os.path.getmtime(out)
+    deps = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + \
+        [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
+    return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build(force: bool = False, ptxas_info: bool = False, out: str = LIB) -> str:
+    if force or ptxas_info or _stale(out):
+        tmp = out + ".tmp%d" % os.getpid()
+        subprocess.run(command(tmp, ptxas_info), check=True)
+        os.replace(tmp, out)
+    return out
+
+
+if __name__ == "__main__":
+    print(build(force=True, ptxas_info="--ptxas-info" in sys.argv))

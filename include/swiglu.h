@@ -1,0 +1,114 @@
+/*
+ * swiglu.h -- C ABI of libswiglu, the fused gate-up SwiGLU for GB300 (sm_103a).
+ *
+ * The operation (Liger-Kernel Megatron SwiGLU page, §Background): Megatron's
+ * linear_fc1 produces a single [s, b, 2n] (or [tokens, 2n]) buffer x whose
+ * columns [0, n) hold the gate g and columns [n, 2n) the up projection u.  The
+ * fused kernels read both halves of each row through a column offset into that
+ * one buffer -- no chunk, copy or concatenation.  3D inputs are passed as
+ * rows = s * b rows of one common row stride (§Megatron feature compatibility:
+ * 2D and 3D inputs).
+ *
+ *   forward   y[r, j]      = silu(g) * u,  silu(g) = g * sigmoid(g)
+ *   backward  dx[r, j]     = dy[r, j] * u * s * (1 + g * (1 - s))    (d gate)
+ *             dx[r, n + j] = dy[r, j] * g * s                        (d up)
+ *   with g = x[r, j], u = x[r, n + j], s = sigmoid(g), 0 <= j < n.
+ *
+ * The backward recomputes the sigmoid from the saved fc1 buffer and may write
+ * its result over that buffer (§Optional: in_place=True).  The page prints no
+ * backward formula; the one above is the analytic derivative of silu(g) * u.
+ * bias is not supported (§Scope: bias=None).
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are DEVICE pointers owned by the caller.  The library never
+ *     allocates, frees or retains memory and keeps no per-call state.
+ *   - Sizes and row strides are counted in ELEMENTS of the dtype; within a row
+ *     elements are contiguous.  Row r of x starts at x + r * x_row_stride.
+ *   - All tensors of one call share one dtype.  Arithmetic is fp32; each result
+ *     is rounded once to the dtype (round to nearest even).
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and runs
+ *     asynchronously; the call returns after the launch.  The current CUDA
+ *     device must be the one that owns the pointers.
+ *   - Every argument is checked on the host before anything is launched; on
+ *     any error nothing is written and nothing is launched.  rows == 0 or
+ *     n == 0 is a valid empty call (returns SWIGLU_OK, touches nothing, and
+ *     accepts NULL pointers).
+ */
+#ifndef LIBSWIGLU_SWIGLU_H
+#define LIBSWIGLU_SWIGLU_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream (a pointer to the driver's stream
+ * object), declared here so that this header does not need the CUDA headers. */
+typedef struct CUstream_st *swiglu_stream_t;
+
+typedef enum {
+    SWIGLU_F32 = 0,  /* IEEE binary32 */
+    SWIGLU_BF16 = 1  /* bfloat16: top 16 bits of a binary32 */
+} swiglu_dtype_t;
+
+typedef enum {
+    SWIGLU_OK = 0,
+    SWIGLU_ERR_NULL = -1,   /* a required pointer is NULL                       */
+    SWIGLU_ERR_DTYPE = -2,  /* dtype is not a swiglu_dtype_t value              */
+    SWIGLU_ERR_SHAPE = -3,  /* rows or n negative, or n > SWIGLU_MAX_N, or the
+                               byte extent of a tensor overflows int64          */
+    SWIGLU_ERR_STRIDE = -4, /* a row stride is shorter than its row             */
+    SWIGLU_ERR_ALIAS = -5,  /* an output overlaps an input it must not overlap  */
+    SWIGLU_ERR_CUDA = -6    /* the CUDA runtime reported an error; see
+                               swiglu_last_cuda_error()                         */
+} swiglu_status_t;
+
+/* Largest supported n (columns per half). */
+#define SWIGLU_MAX_N ((int64_t)1 << 30)
+
+/*
+ * Forward: y[r, j] = silu(x[r, j]) * x[r, n + j] for r < rows, j < n.
+ *   x  [rows, 2n], row stride x_row_stride >= 2n   (read only)
+ *   y  [rows, n],  row stride y_row_stride >= n    (written)
+ * The byte range spanned by y must not overlap the one spanned by x
+ * (SWIGLU_ERR_ALIAS).
+ */
+swiglu_status_t swiglu_gateup_fwd(const void *x, void *y, int64_t rows, int64_t n,
+                                  int64_t x_row_stride, int64_t y_row_stride,
+                                  swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+/*
+ * Backward: dx[r, j] = d gate, dx[r, n + j] = d up (formulas above).
+ *   dy [rows, n],  row stride dy_row_stride >= n   (read only)
+ *   x  [rows, 2n], row stride x_row_stride >= 2n   (the saved fc1 buffer)
+ *   dx [rows, 2n], row stride dx_row_stride >= 2n  (written)
+ * in_place == 0: dx must not overlap x or dy (SWIGLU_ERR_ALIAS).
+ * in_place != 0: the gradient is written over x.  dx must be NULL or equal to
+ *   x (else SWIGLU_ERR_ALIAS) and dx_row_stride must be 0 or equal to
+ *   x_row_stride (else SWIGLU_ERR_STRIDE); dy must not overlap x
+ *   (SWIGLU_ERR_ALIAS).  The in-place result is bit-identical to the
+ *   out-of-place one.  Afterwards x no longer holds the forward input: a second
+ *   backward over the same buffer computes garbage, which the library cannot
+ *   detect (the caller must guard against it, as the page's known issue 1 says).
+ */
+swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64_t rows,
+                                  int64_t n, int64_t dy_row_stride, int64_t x_row_stride,
+                                  int64_t dx_row_stride, swiglu_dtype_t dtype, int in_place,
+                                  swiglu_stream_t stream);
+
+/* Static English text for a status code; never NULL. */
+const char *swiglu_status_string(swiglu_status_t status);
+
+/* The cudaError_t value behind the calling thread's most recent
+ * SWIGLU_ERR_CUDA (0 if there was none). */
+int swiglu_last_cuda_error(void);
+
+/* ABI version: incremented when a signature or a convention above changes. */
+int swiglu_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSWIGLU_SWIGLU_H */

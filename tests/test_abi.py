@@ -1,0 +1,123 @@
+"""Host-side tests of the C ABI: the library loads, exports what the header
+declares, and rejects bad arguments before touching the GPU (so these run on a
+machine without one).  Pointers here are plain integers that are never
+dereferenced: every call below fails validation first."""
+import os
+import re
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swiglu.h")
+
+
+@pytest.fixture(scope="module")
+def sw():
+    from gate_up_swiglu_gb300 import build
+
+    build.build()
+    import gate_up_swiglu_gb300 as sw
+
+    return sw
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swiglu_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_calls():
+    assert declared_functions() == sorted(
+        ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_status_string",
+         "swiglu_last_cuda_error", "swiglu_abi_version"])
+
+
+def test_library_exports_every_declared_symbol(sw):
+    for name in declared_functions():
+        assert hasattr(sw.lib, name), name
+    assert set(sw.EXPORTS) == set(declared_functions())
+    nm = shutil.which("nm")
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", sw.LIB_PATH], capture_output=True,
+                             text=True, check=True).stdout
+        for name in declared_functions():
+            assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_status_strings(sw):
+    for code in range(-6, 1):
+        s = sw.status_string(code)
+        assert s and s != "unknown status"
+    assert sw.status_string(-99) == "unknown status"
+    assert sw.lib.swiglu_abi_version() == 1
+    assert sw.lib.swiglu_last_cuda_error() == 0
+
+
+# fake, never-dereferenced device addresses, 256-byte aligned and far apart
+X, Y, DY, DX = 0x10_0000_0000, 0x20_0000_0000, 0x30_0000_0000, 0x40_0000_0000
+F32, BF16 = 0, 1
+
+
+def fwd(sw, x=X, y=Y, rows=4, n=8, sx=16, sy=8, dt=BF16):
+    return sw.lib.swiglu_gateup_fwd(x, y, rows, n, sx, sy, dt, None)
+
+
+def bwd(sw, dy=DY, x=X, dx=DX, rows=4, n=8, sdy=8, sx=16, sdx=16, dt=BF16, ip=0):
+    return sw.lib.swiglu_gateup_bwd(dy, x, dx, rows, n, sdy, sx, sdx, dt, ip, None)
+
+
+def test_empty_calls_are_noops(sw):
+    assert fwd(sw, x=None, y=None, rows=0) == 0
+    assert fwd(sw, x=None, y=None, n=0) == 0
+    assert bwd(sw, dy=None, x=None, dx=None, rows=0) == 0
+    assert bwd(sw, dy=None, x=None, dx=None, n=0, ip=1) == 0
+
+
+def test_fwd_rejections(sw):
+    assert fwd(sw, dt=7) == -2
+    assert fwd(sw, dt=-1) == -2
+    assert fwd(sw, rows=-1) == -3
+    assert fwd(sw, n=-1) == -3
+    assert fwd(sw, n=(1 << 30) + 1, sx=1 << 32, sy=1 << 31) == -3
+    assert fwd(sw, x=None) == -1
+    assert fwd(sw, y=None) == -1
+    assert fwd(sw, sx=15) == -4
+    assert fwd(sw, sy=7) == -4
+    # extent overflows int64
+    assert fwd(sw, rows=1 << 40, sx=1 << 40) == -3
+    # y inside x's span, or x inside y's
+    assert fwd(sw, y=X + 2 * 16 * 3) == -5
+    assert fwd(sw, y=X - 2) == -5
+
+
+def test_bwd_rejections(sw):
+    assert bwd(sw, dt=3) == -2
+    assert bwd(sw, rows=-5) == -3
+    assert bwd(sw, dy=None) == -1
+    assert bwd(sw, x=None) == -1
+    assert bwd(sw, dx=None) == -1
+    assert bwd(sw, sdy=7) == -4
+    assert bwd(sw, sx=15) == -4
+    assert bwd(sw, sdx=10) == -4
+    # out of place: dx may not overlap x or dy
+    assert bwd(sw, dx=X) == -5
+    assert bwd(sw, dx=X + 8) == -5
+    assert bwd(sw, dx=DY + 4) == -5
+    # in place: dx must be x (or NULL) with x's stride, dy may not overlap x
+    assert bwd(sw, ip=1, dx=DX) == -5
+    assert bwd(sw, ip=1, dx=X, sdx=24) == -4
+    assert bwd(sw, ip=1, dx=X, dy=X + 16) == -5
+
+
+def test_import_fails_loudly_without_the_library(tmp_path):
+    pkg = os.path.join(ROOT, "gate_up_swiglu_gb300")
+    dst = tmp_path / "gate_up_swiglu_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("*.so", "__pycache__", "csrc"))
+    code = "import gate_up_swiglu_gb300"
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode != 0
+    assert "libswiglu.so is not built" in r.stderr

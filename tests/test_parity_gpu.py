@@ -1,0 +1,266 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Tolerances (tests/helpers.py): fp32 within max(2e-6 relative, 1e-7 absolute) of
+the oracle's once-rounded fp64 result; bf16 within one bf16 step; the in-place
+backward bit-identical to the out-of-place one.
+
+Sizes: the tiny, Megatron-shape and odd-width workloads are compared in full;
+the large-FFN and Llama-like workloads run at full size (the launch
+configuration the bench times) and are compared on sampled whole rows, plus
+bitwise in-place/out-of-place equality over the whole tensor.  Smaller ragged
+cases cover every pack width (16/8/4/2 bytes and single elements), padded row
+strides, misaligned base pointers and guard bands around every buffer.
+"""
+import os
+
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import assert_bitwise, assert_parity
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def sw():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gate_up_swiglu_gb300 import build
+
+    build.build()
+    import gate_up_swiglu_gb300 as sw
+
+    return sw
+
+
+def _run_all(sw, x, dy):
+    """fwd, out-of-place bwd, in-place bwd on the GPU; x, dy are 2D device tensors."""
+    y = sw.swiglu_gateup_fwd(x)
+    dx = sw.swiglu_gateup_bwd(dy, x)
+    xi = x.clone()
+    sw.swiglu_gateup_bwd(dy, xi, in_place=True)
+    torch.cuda.synchronize()
+    return y, dx, xi
+
+
+def _check_rows(x, dy, y, dx, rows_idx, what):
+    xs = x[rows_idx].cpu()
+    dys = dy[rows_idx].cpu()
+    assert_parity(y[rows_idx], oracle.fwd(xs), f"{what} fwd")
+    assert_parity(dx[rows_idx], oracle.bwd(dys, xs), f"{what} bwd")
+
+
+# ------------------------------------------------------- whole workloads ---
+
+@pytest.mark.parametrize("name", ["tiny_f32", "megatron_4096_bf16", "odd_5503_f32"])
+def test_workload_full_compare(sw, name):
+    w = W.WORKLOADS[name]
+    x, dy = W.make_inputs(w, "cpu")
+    y, dx, xi = _run_all(sw, x.cuda(), dy.cuda())
+    assert_parity(y, oracle.fwd(x), f"{name} fwd", extra=x[:, :w.n])
+    ref_dx = oracle.bwd(dy, x)
+    assert_parity(dx, ref_dx, f"{name} bwd")
+    assert_bitwise(xi, dx, f"{name} in-place vs out-of-place")
+
+
+@pytest.mark.parametrize("name", ["large_32768_bf16", "llama_14336_bf16_2d"])
+def test_workload_full_size_sampled(sw, name):
+    w = W.WORKLOADS[name]
+    x, dy = W.make_inputs(w, "cuda")
+    y, dx, xi = _run_all(sw, x, dy)
+    assert_bitwise(xi, dx, f"{name} in-place vs out-of-place")
+    del xi
+    g = torch.Generator().manual_seed(99)
+    rows = torch.randperm(w.rows, generator=g)[:40].tolist() + [0, 1, w.rows - 2, w.rows - 1]
+    idx = torch.tensor(sorted(set(rows)), device="cuda")
+    _check_rows(x, dy, y, dx, idx, name)
+    # a property at full size: finite inputs give finite outputs
+    assert bool(torch.isfinite(y).all()) and bool(torch.isfinite(dx).all())
+
+
+def test_3d_inputs_flatten(sw):
+    w = W.WORKLOADS["megatron_4096_bf16"]
+    x, dy = W.make_inputs(w, "cuda", rows=64)
+    x3 = x.contiguous().view(16, 4, 2 * w.n)
+    dy3 = dy.view(16, 4, w.n)
+    y3 = sw.swiglu_gateup_fwd(x3)
+    dx3 = sw.swiglu_gateup_bwd(dy3, x3)
+    assert y3.shape == (16, 4, w.n) and dx3.shape == x3.shape
+    assert_bitwise(y3.view(64, w.n), sw.swiglu_gateup_fwd(x), "3D vs 2D fwd")
+    assert_bitwise(dx3.view(64, 2 * w.n), sw.swiglu_gateup_bwd(dy, x), "3D vs 2D bwd")
+
+
+# ------------------------------------------------------ exhaustive sweeps ---
+
+def _bf16_all_patterns():
+    b = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    return b.view(torch.bfloat16)
+
+
+def test_bf16_every_gate_value(sw):
+    """All 65536 bf16 gate bit patterns (NaN and inf included) x varied up/dy."""
+    gates = _bf16_all_patterns().view(8, 8192)
+    n = 8192
+    gen = torch.Generator().manual_seed(7)
+    for scale in (1.0, 64.0):
+        up = (torch.randn(8, n, generator=gen) * scale).to(torch.bfloat16)
+        dy = (torch.randn(8, n, generator=gen) * scale).to(torch.bfloat16)
+        x = torch.cat([gates, up], dim=1)
+        y, dx, xi = _run_all(sw, x.cuda(), dy.cuda())
+        assert_parity(y, oracle.fwd(x), "bf16 sweep fwd", extra=gates)
+        assert_parity(dx, oracle.bwd(dy, x), "bf16 sweep bwd")
+        assert_bitwise(xi, dx, "bf16 sweep in-place")
+
+
+@pytest.mark.parametrize("lo,hi", [(-1.6, -1.0), (-0.02, 0.02), (8.0, 24.0), (-24.0, -8.0),
+                                   (-105.0, -80.0), (80.0, 105.0), (-1e6, 1e6)])
+def test_f32_dense_gate_ranges(sw, lo, hi):
+    """Dense fp32 gate grids over the ranges where the arithmetic is delicate:
+    the root of silu' (-1.28), zero, the sigmoid tails and the ends of the fp32
+    exponential's range."""
+    m = 1 << 20
+    g = torch.linspace(lo, hi, m, dtype=torch.float64).float()
+    gen = torch.Generator().manual_seed(11)
+    up = torch.rand(m, generator=gen) * 8 - 4
+    dy = torch.randn(m, generator=gen) * 3
+    n = 4096
+    x = torch.cat([g.view(-1, n), up.view(-1, n)], dim=1)
+    dy = dy.view(-1, n)
+    y, dx, xi = _run_all(sw, x.cuda(), dy.cuda())
+    assert_parity(y, oracle.fwd(x), f"f32 [{lo},{hi}] fwd", extra=x[:, :n])
+    assert_parity(dx, oracle.bwd(dy, x), f"f32 [{lo},{hi}] bwd")
+    assert_bitwise(xi, dx, "f32 sweep in-place")
+
+
+def _read_golden():
+    path = os.path.join(HERE, "golden", "oracle_specials.txt")
+    lines = [l for l in open(path).read().splitlines() if l and not l.startswith("#")]
+    out = {}
+    for head, body in zip(lines[::2], lines[1::2]):
+        dt, name, r, c = head.split()
+        vals = [int(v, 16) for v in body.split()]
+        if dt == "f32":
+            t = torch.tensor(vals, dtype=torch.int64).to(torch.int32).view(torch.float32)
+        else:
+            t = torch.tensor(vals, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+        out[(dt, name)] = t.view(int(r), int(c))
+    return out
+
+
+def test_golden_special_values(sw):
+    gold = _read_golden()
+    for dt in ("f32", "bf16"):
+        x, dy = gold[(dt, "x")], gold[(dt, "dy")]
+        y, dx, xi = _run_all(sw, x.cuda(), dy.cuda())
+        assert_parity(y, gold[(dt, "y")], f"golden {dt} fwd", extra=x[:, : x.shape[1] // 2])
+        assert_parity(dx, gold[(dt, "dx")], f"golden {dt} bwd")
+        assert_bitwise(xi, dx, f"golden {dt} in-place")
+
+
+# ------------------------------------- pack widths, strides, guard bands ---
+
+SENTINEL_F32 = -12345.5
+CASES = [
+    # (dtype, rows, n, x_pad, y_pad, dy_pad, dx_pad, misalign_elems)
+    ("bf16", 37, 4096, 0, 0, 0, 0, 0),    # 16-byte packs
+    ("bf16", 37, 4100, 0, 0, 0, 0, 0),    # 8-byte packs (n % 8 == 4)
+    ("bf16", 29, 4098, 0, 0, 0, 0, 0),    # 4-byte packs (n % 4 == 2)
+    ("bf16", 31, 1001, 0, 0, 0, 0, 0),    # single elements (odd n)
+    ("bf16", 23, 2048, 8, 16, 8, 24, 0),  # padded strides keep 16-byte packs
+    ("bf16", 23, 2048, 2, 6, 2, 4, 0),    # padding drops to 4-byte packs
+    ("bf16", 19, 2048, 0, 0, 0, 0, 1),    # misaligned base pointers
+    ("bf16", 3000, 8, 0, 0, 0, 0, 0),     # many short rows (grid-stride, row carry)
+    ("bf16", 5, 1, 0, 0, 0, 0, 0),        # n = 1
+    ("f32", 37, 4096, 0, 0, 0, 0, 0),     # 16-byte packs
+    ("f32", 37, 4098, 0, 0, 0, 0, 0),     # 8-byte packs
+    ("f32", 31, 5503, 0, 0, 0, 0, 0),     # odd n
+    ("f32", 23, 1024, 4, 12, 4, 8, 0),    # padded strides, 16-byte packs
+    ("f32", 23, 1024, 1, 3, 1, 2, 1),     # odd strides and misaligned pointers
+    ("f32", 40000, 3, 0, 0, 0, 0, 0),     # many tiny rows
+    ("f32", 1, 70000, 0, 0, 0, 0, 0),     # one long row
+]
+
+
+def _guarded(rows, cols, pad, misalign, dtype, fill, guard=64):
+    """A [rows, cols] view with row stride cols + pad, inside a buffer with
+    `guard` sentinel elements on both sides; returns (buffer, view, offset)."""
+    stride = cols + pad
+    total = guard + misalign + rows * stride + guard
+    buf = torch.full((total,), fill, dtype=dtype, device="cuda")
+    off = guard + misalign
+    view = buf[off: off + rows * stride].view(rows, stride)[:, :cols]
+    return buf, view
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-r{c[1]}-n{c[2]}-p{c[3]}{c[4]}{c[5]}{c[6]}-m{c[7]}"
+                                             for c in CASES])
+def test_layouts_and_guard_bands(sw, case):
+    dts, rows, n, xp, yp, dyp, dxp, mis = case
+    dt = torch.float32 if dts == "f32" else torch.bfloat16
+    gen = torch.Generator().manual_seed(rows * 7 + n)
+    x_cpu = (torch.randn(rows, 2 * n, generator=gen) * 3).to(dt)
+    dy_cpu = torch.randn(rows, n, generator=gen).to(dt)
+    xb, x = _guarded(rows, 2 * n, xp, mis, dt, float("nan"))
+    dyb, dy = _guarded(rows, n, dyp, mis, dt, float("nan"))
+    yb, y = _guarded(rows, n, yp, mis, dt, SENTINEL_F32)
+    dxb, dx = _guarded(rows, 2 * n, dxp, mis, dt, SENTINEL_F32)
+    x.copy_(x_cpu)
+    dy.copy_(dy_cpu)
+    xb0, yb0, dxb0 = xb.clone(), yb.clone(), dxb.clone()
+    sw.swiglu_gateup_fwd(x, y)
+    sw.swiglu_gateup_bwd(dy, x, dx)
+    torch.cuda.synchronize()
+    assert_parity(y, oracle.fwd(x_cpu), "fwd")
+    assert_parity(dx, oracle.bwd(dy_cpu, x_cpu), "bwd")
+    assert_bitwise(xb, xb0, "x buffer (read-only) changed")
+    # everything outside the written views keeps its sentinel: refill the
+    # views and the whole buffers must be back to their initial bits
+    y.fill_(SENTINEL_F32)
+    assert_bitwise(yb, yb0, "y guard bands / padding")
+    dx_after = dx.clone()
+    dx.fill_(SENTINEL_F32)
+    assert_bitwise(dxb, dxb0, "dx guard bands / padding")
+    # in place over the guarded x: same bits as the out-of-place result, and
+    # x's padding and guards untouched
+    sw.swiglu_gateup_bwd(dy, x, in_place=True)
+    torch.cuda.synchronize()
+    assert_bitwise(x, dx_after, "in-place vs out-of-place")
+    x.copy_(x_cpu)
+    assert_bitwise(xb, xb0, "x guard bands / padding after in-place")
+
+
+# ------------------------------------------------------------ API surface ---
+
+def test_empty_and_errors(sw):
+    dt = torch.bfloat16
+    x = torch.empty(0, 16, dtype=dt, device="cuda")
+    assert sw.swiglu_gateup_fwd(x).shape == (0, 8)
+    assert sw.swiglu_gateup_bwd(torch.empty(0, 8, dtype=dt, device="cuda"), x).shape == (0, 16)
+    x = torch.randn(4, 16, device="cuda").to(dt)
+    # y overlapping x is rejected and nothing is written
+    before = x.clone()
+    with pytest.raises(sw.SwigluError) as e:
+        sw.swiglu_gateup_fwd(x, x[:, :8])
+    assert e.value.status == -5
+    assert_bitwise(x, before, "rejected call wrote")
+    with pytest.raises(sw.SwigluError) as e:
+        sw.swiglu_gateup_bwd(x[:, :8].contiguous(), x, x)
+    assert e.value.status == -5
+    assert sw.lib.swiglu_last_cuda_error() == 0
+
+
+def test_side_stream(sw):
+    w = W.WORKLOADS["megatron_4096_bf16"]
+    x, dy = W.make_inputs(w, "cuda", rows=256)
+    ref = sw.swiglu_gateup_bwd(dy, x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = sw.swiglu_gateup_fwd(x)
+        dx = sw.swiglu_gateup_bwd(dy, x)
+    s.synchronize()
+    assert_bitwise(dx, ref, "side stream")
+    assert_bitwise(y, sw.swiglu_gateup_fwd(x), "side stream fwd")
