@@ -239,9 +239,13 @@ def ours_arm(args, w):
         dist.init_process_group(backend="nccl", device_id=dev)
         pg = dist
 
-    from gate_up_swiglu_gb300 import build
+    import importlib.util
 
-    build.build()
+    spec = importlib.util.spec_from_file_location(
+        "_libswiglu_build", os.path.join(ROOT, "gate_up_swiglu_gb300", "build.py"))
+    builder = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(builder)
+    builder.build()
     import gate_up_swiglu_gb300 as sw
 
     def barrier():

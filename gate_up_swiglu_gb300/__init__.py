@@ -45,7 +45,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"libswiglu.so is not built ({LIB_PATH} missing); build it with "
-            "`python -m gate_up_swiglu_gb300.build` or __graft_entry__.build()")
+            "`python gate_up_swiglu_gb300/build.py` or __graft_entry__.build()")
     lib = ctypes.CDLL(LIB_PATH)
     i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.swiglu_gateup_fwd.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]

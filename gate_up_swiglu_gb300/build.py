@@ -1,6 +1,9 @@
 """Compile libswiglu.so for sm_103a with nvcc, in-tree.
 
-    python -m gate_up_swiglu_gb300.build [--ptxas-info]
+    python gate_up_swiglu_gb300/build.py [--ptxas-info]
+
+Run it as a script (or load it by path): importing the package itself needs
+the built library.
 
 The library is one translation unit (the C ABI plus the kernel templates it
 instantiates), linked against the static CUDA runtime so the .so depends on

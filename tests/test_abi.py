@@ -16,9 +16,9 @@ HEADER = os.path.join(ROOT, "include", "swiglu.h")
 
 @pytest.fixture(scope="module")
 def sw():
-    from gate_up_swiglu_gb300 import build
+    from conftest import build_library
 
-    build.build()
+    build_library()
     import gate_up_swiglu_gb300 as sw
 
     return sw

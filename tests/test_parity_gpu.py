@@ -29,9 +29,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 def sw():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
-    from gate_up_swiglu_gb300 import build
+    from conftest import build_library
 
-    build.build()
+    build_library()
     import gate_up_swiglu_gb300 as sw
 
     return sw
