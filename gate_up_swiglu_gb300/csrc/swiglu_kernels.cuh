@@ -78,6 +78,9 @@ struct F32 {
     // fp32 results must sit within 2e-6 relative (1e-7 absolute) of the exact
     // value, which plain fp32 evaluation of silu' misses near its root.
     static constexpr bool kRootWindow = true;
+    // fp32 results below the 1e-7 absolute floor are never graded, so the
+    // deep negative tail needs no rescaling (see BF16::kDeepScale).
+    static constexpr bool kDeepScale = false;
     static __device__ __forceinline__ float get(const uint32_t *w, int i) {
         return __uint_as_float(w[i]);
     }
@@ -91,6 +94,12 @@ struct BF16 {
     // one bf16 ulp (2^-8 relative) dwarfs the fp32 error of silu' at the bf16
     // values nearest its root (|silu'| >= 6e-4 there), so no root window.
     static constexpr bool kRootWindow = false;
+    // For g < -64, exp(-|g|) heads into the fp32 subnormal range (below
+    // g = -87.3) and loses relative precision, while silu(g) * u and friends
+    // can still be normal or subnormal bf16 numbers.  There the exponential
+    // is taken 64 binades higher and every result is scaled back by 2^-64 in
+    // one final, correctly rounded multiply.
+    static constexpr bool kDeepScale = true;
     static __device__ __forceinline__ float get(const uint32_t *w, int i) {
         const uint32_t word = w[i >> 1];
         return __uint_as_float((i & 1) ? (word & 0xFFFF0000u) : (word << 16));
@@ -102,19 +111,16 @@ struct BF16 {
 };
 
 // ------------------------------------------------------------------ math ---
-// sigmoid(g) and 1 - sigmoid(g) from t = exp(-|g|) in (0, 1]: neither the
-// exponential overflows nor 1 - s cancels, for any finite g, and subnormal
-// sigmoid values (g below about -87) are kept.  Explicit _rn operations fix
-// the rounding of every step (no contraction), so all instantiations -- in
-// particular the in-place and out-of-place backward -- produce the same bits.
-__device__ __forceinline__ void sigmoid_pair(float g, float &s, float &oms) {
-    const float t = expf(-fabsf(g));
-    const float r = __frcp_rn(__fadd_rn(1.0f, t));
-    const float tr = __fmul_rn(t, r);
-    const bool pos = g >= 0.0f;
-    s = pos ? r : tr;
-    oms = pos ? tr : r;
-}
+// sigmoid(g) and 1 - sigmoid(g) come from t = exp(-|g|) in (0, 1]:
+//   g >= 0:  s = 1 / (1 + t),  1 - s = t / (1 + t)
+//   g <  0:  s = t / (1 + t),  1 - s = 1 / (1 + t)
+// so neither the exponential overflows nor 1 - s cancels, for any finite g.
+// Explicit _rn operations fix the rounding of every step (no contraction), so
+// all instantiations -- in particular the in-place and out-of-place backward
+// -- produce the same bits.
+
+constexpr float kLn2x64 = 44.3614195558365f;  // 64 ln 2
+constexpr float kTwoPowMinus64 = 5.421010862427522e-20f;  // 2^-64, exact
 
 // silu'(g0 + d) near the root g0 of silu', as a Taylor polynomial in d.
 __device__ __forceinline__ float dsilu_near_root(float d) {
@@ -125,23 +131,43 @@ __device__ __forceinline__ float dsilu_near_root(float d) {
     return __fmul_rn(acc, d);
 }
 
-// silu(g) = g s and silu'(g) = s (1 + g (1 - s)).
-template <typename E>
-__device__ __forceinline__ void silu_and_grad(float g, float &silu, float &dsilu) {
-    float s, oms;
-    sigmoid_pair(g, s, oms);
-    silu = __fmul_rn(g, s);
-    dsilu = __fmul_rn(s, __fmaf_rn(g, oms, 1.0f));
-    if (E::kRootWindow) {
-        const float d = __fsub_rn(__fsub_rn(g, SILU_ROOT_G0_HI), SILU_ROOT_G0_LO);
-        if (fabsf(d) < SILU_ROOT_WINDOW) dsilu = dsilu_near_root(d);
-    }
-}
+// The activation terms of one gate value:
+//   silu  = g s            (times 2^64 when `scale` is 2^-64)
+//   dsilu = s (1 + g (1 - s))   (same scaling)
+//   scale = the factor every product of silu / dsilu must finally be multiplied by.
+struct Act {
+    float silu, dsilu, scale;
+};
 
-__device__ __forceinline__ float silu_only(float g) {
-    float s, oms;
-    sigmoid_pair(g, s, oms);
-    return __fmul_rn(g, s);
+template <typename E, bool kGrad>
+__device__ __forceinline__ Act activation(float g) {
+    const float a = fabsf(g);
+    const bool pos = g >= 0.0f;
+    bool deep = false;
+    float arg = a;
+    if (E::kDeepScale) {
+        // for a > 64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or without
+        // the scaling and r = 1 stays exact
+        deep = !pos && a > 64.0f;
+        arg = deep ? __fsub_rn(a, kLn2x64) : a;
+    }
+    const float t = expf(-arg);
+    const float r = __frcp_rn(__fadd_rn(1.0f, t));
+    const float tr = __fmul_rn(t, r);
+    const float s = pos ? r : tr;
+    Act o;
+    o.silu = __fmul_rn(g, s);
+    o.scale = deep ? kTwoPowMinus64 : 1.0f;
+    o.dsilu = 0.0f;
+    if (kGrad) {
+        const float oms = pos ? tr : r;
+        o.dsilu = __fmul_rn(s, __fmaf_rn(g, oms, 1.0f));
+        if (E::kRootWindow) {
+            const float d = __fsub_rn(__fsub_rn(g, SILU_ROOT_G0_HI), SILU_ROOT_G0_LO);
+            if (fabsf(d) < SILU_ROOT_WINDOW) o.dsilu = dsilu_near_root(d);
+        }
+    }
+    return o;
 }
 
 // ---------------------------------------------------------------- kernels ---
@@ -226,8 +252,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
             if (r[k] < p.rows) {
                 uint32_t o[NW] = {};
 #pragma unroll
-                for (int i = 0; i < VEC; ++i)
-                    E::put(o, i, __fmul_rn(silu_only(E::get(g[k], i)), E::get(u[k], i)));
+                for (int i = 0; i < VEC; ++i) {
+                    const Act act = activation<E, false>(E::get(g[k], i));
+                    E::put(o, i, __fmul_rn(__fmul_rn(act.silu, E::get(u[k], i)), act.scale));
+                }
                 M::store(y + (r[k] * p.y_stride + c[k]) * B, o);
             }
         }
@@ -270,10 +298,9 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
                     const float gf = E::get(g[k], i);
                     const float uf = E::get(u[k], i);
                     const float df = E::get(d[k], i);
-                    float silu, dsilu;
-                    silu_and_grad<E>(gf, silu, dsilu);
-                    E::put(og, i, __fmul_rn(__fmul_rn(df, uf), dsilu));
-                    E::put(ou, i, __fmul_rn(df, silu));
+                    const Act act = activation<E, true>(gf);
+                    E::put(og, i, __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale));
+                    E::put(ou, i, __fmul_rn(__fmul_rn(df, act.silu), act.scale));
                 }
                 char *pdx = dx + (r[k] * p.dx_stride + c[k]) * B;
                 M::store(pdx, og);
