@@ -51,10 +51,10 @@ bool span_of(const void *p, int64_t rows, int64_t cols, int64_t stride, int eb, 
 
 bool overlaps(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
 
-// Widest pack (16, 8, 4 or 2 bytes) that divides n, every row stride and
+// Widest pack (32, 16, 8, 4 or 2 bytes) that divides n, every row stride and
 // every base address; returns the number of elements per pack.
 int pick_vec(int eb, int64_t n, const int64_t *strides, int ns, const void *const *ptrs, int np) {
-    for (int bytes = 16; bytes > eb; bytes /= 2) {
+    for (int bytes = 32; bytes > eb; bytes /= 2) {
         const int vec = bytes / eb;
         bool ok = (n % vec) == 0;
         for (int i = 0; ok && i < ns; ++i) ok = (strides[i] % vec) == 0;
@@ -64,10 +64,19 @@ int pick_vec(int eb, int64_t n, const int64_t *strides, int ns, const void *cons
     return 1;
 }
 
-// Packs in flight per operand per thread: 32 bytes' worth, at least 2, at most 8.
+// Packs in flight per operand per thread: one 32-byte pack, two 16-byte
+// packs, four 8-byte packs, else eight (measured on GB300: more unrolling of
+// 32-byte packs costs occupancy and loses).
 constexpr int unroll_for(int pack_bytes) {
-    return pack_bytes >= 16 ? 2 : (pack_bytes >= 8 ? 4 : 8);
+    return pack_bytes >= 32 ? 1 : (pack_bytes >= 16 ? 2 : (pack_bytes >= 8 ? 4 : 8));
 }
+
+// Cache behaviour: inputs of the out-of-place kernels go through the
+// read-only path without L1 allocation; the in-place backward reads what it
+// writes, so it uses coherent loads.  Outputs are streaming stores.
+constexpr int kLoadOutOfPlace = swiglu::kLdNC;
+constexpr int kLoadInPlace = swiglu::kLdNoAlloc;
+constexpr int kStore = swiglu::kStStream;
 
 struct Device {
     int id;
@@ -121,7 +130,7 @@ swiglu_status_t launch_fwd(const void *x, void *y, int64_t rows, int64_t n, int6
                            int64_t sy, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
-    auto kernel = swiglu::swiglu_fwd_kernel<E, VEC, U>;
+    auto kernel = swiglu::swiglu_fwd_kernel<E, VEC, U, kLoadOutOfPlace, kStore>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -150,7 +159,8 @@ swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows
                            int64_t sdy, int64_t sx, int64_t sdx, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
-    auto kernel = swiglu::swiglu_bwd_kernel<E, VEC, U, IN_PLACE>;
+    auto kernel = swiglu::swiglu_bwd_kernel<E, VEC, U, IN_PLACE,
+                                            IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -180,7 +190,8 @@ template <typename E>
 swiglu_status_t dispatch_fwd(int vec, const void *x, void *y, int64_t rows, int64_t n, int64_t sx,
                              int64_t sy, cudaStream_t st) {
     switch (vec) {
-        case 8: if constexpr (E::kBytes == 2) return launch_fwd<E, 8>(x, y, rows, n, sx, sy, st); break;
+        case 16: if constexpr (E::kBytes == 2) return launch_fwd<E, 16>(x, y, rows, n, sx, sy, st); break;
+        case 8: return launch_fwd<E, 8>(x, y, rows, n, sx, sy, st);
         case 4: return launch_fwd<E, 4>(x, y, rows, n, sx, sy, st);
         case 2: return launch_fwd<E, 2>(x, y, rows, n, sx, sy, st);
         default: break;
@@ -192,10 +203,11 @@ template <typename E, bool IP>
 swiglu_status_t dispatch_bwd(int vec, const void *dy, const void *x, void *dx, int64_t rows,
                              int64_t n, int64_t sdy, int64_t sx, int64_t sdx, cudaStream_t st) {
     switch (vec) {
-        case 8:
+        case 16:
             if constexpr (E::kBytes == 2)
-                return launch_bwd<E, 8, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
+                return launch_bwd<E, 16, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
             break;
+        case 8: return launch_bwd<E, 8, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
         case 4: return launch_bwd<E, 4, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
         case 2: return launch_bwd<E, 2, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
         default: break;

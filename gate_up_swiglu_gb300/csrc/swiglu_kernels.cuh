@@ -27,49 +27,113 @@ namespace swiglu {
 constexpr int kThreads = 256;
 
 // ---------------------------------------------------------------- memory ---
-// Streaming loads/stores of one B-byte pack, viewed as 32-bit words
-// (a 2-byte pack uses the low half of word 0).
-template <int B>
-struct Mem;
+// Loads and stores of one B-byte pack (B = 32, 16, 8, 4 or 2), viewed as
+// 32-bit words (a 2-byte pack uses the low half of word 0).  32-byte packs use
+// the 256-bit global accesses of sm_100-class GPUs.  The cache behaviour is a
+// template parameter:
+//   loads   kLdStream      ld.global.cs            evict-first, coherent
+//           kLdNoAlloc     ld.global.L1::no_allocate                  coherent
+//           kLdNoAlloc256  ... .L2::256B           + 256-byte L2 prefetch
+//           kLdNC          ld.global.nc.L1::no_allocate   read-only path
+//           kLdNC256       ... .L2::256B           + 256-byte L2 prefetch
+//   stores  kStStream      st.global.cs            evict-first
+//           kStNoAlloc     st.global.L1::no_allocate
+//           kStPlain       st.global
+// The read-only (.nc) kinds are only legal when no thread of the kernel writes
+// the loaded memory, i.e. never for the in-place backward.
+enum : int { kLdStream = 0, kLdNoAlloc = 1, kLdNoAlloc256 = 2, kLdNC = 3, kLdNC256 = 4 };
+enum : int { kStStream = 0, kStNoAlloc = 1, kStPlain = 2 };
 
-template <>
-struct Mem<16> {
-    static __device__ __forceinline__ void load(const void *p, uint32_t *w) {
-        const uint4 r = __ldcs(reinterpret_cast<const uint4 *>(p));
-        w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
-    }
-    static __device__ __forceinline__ void store(void *p, const uint32_t *w) {
-        __stcs(reinterpret_cast<uint4 *>(p), make_uint4(w[0], w[1], w[2], w[3]));
-    }
-};
-template <>
-struct Mem<8> {
-    static __device__ __forceinline__ void load(const void *p, uint32_t *w) {
-        const uint2 r = __ldcs(reinterpret_cast<const uint2 *>(p));
-        w[0] = r.x; w[1] = r.y;
-    }
-    static __device__ __forceinline__ void store(void *p, const uint32_t *w) {
-        __stcs(reinterpret_cast<uint2 *>(p), make_uint2(w[0], w[1]));
-    }
-};
-template <>
-struct Mem<4> {
-    static __device__ __forceinline__ void load(const void *p, uint32_t *w) {
-        w[0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
-    }
-    static __device__ __forceinline__ void store(void *p, const uint32_t *w) {
-        __stcs(reinterpret_cast<unsigned int *>(p), w[0]);
-    }
-};
-template <>
-struct Mem<2> {
-    static __device__ __forceinline__ void load(const void *p, uint32_t *w) {
-        w[0] = __ldcs(reinterpret_cast<const unsigned short *>(p));
-    }
-    static __device__ __forceinline__ void store(void *p, const uint32_t *w) {
-        __stcs(reinterpret_cast<unsigned short *>(p), static_cast<unsigned short>(w[0]));
-    }
-};
+template <int B, int KIND>
+struct Ld;
+template <int B, int KIND>
+struct St;
+
+#define SWIGLU_DEFINE_LD(KIND, QUAL)                                                           \
+    template <>                                                                                \
+    struct Ld<32, KIND> {                                                                      \
+        static __device__ __forceinline__ void run(const void *p, uint32_t *w) {               \
+            asm(QUAL ".v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"                          \
+                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),       \
+                  "=r"(w[6]), "=r"(w[7])                                                       \
+                : "l"(p));                                                                     \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct Ld<16, KIND> {                                                                      \
+        static __device__ __forceinline__ void run(const void *p, uint32_t *w) {               \
+            asm(QUAL ".v4.b32 {%0, %1, %2, %3}, [%4];"                                          \
+                : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])                                \
+                : "l"(p));                                                                     \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct Ld<8, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(const void *p, uint32_t *w) {               \
+            asm(QUAL ".v2.b32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));              \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct Ld<4, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(const void *p, uint32_t *w) {               \
+            asm(QUAL ".b32 %0, [%1];" : "=r"(w[0]) : "l"(p));                                   \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct Ld<2, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(const void *p, uint32_t *w) {               \
+            unsigned short h;                                                                  \
+            asm(QUAL ".b16 %0, [%1];" : "=h"(h) : "l"(p));                                      \
+            w[0] = h;                                                                          \
+        }                                                                                      \
+    };
+
+SWIGLU_DEFINE_LD(kLdStream, "ld.global.cs")
+SWIGLU_DEFINE_LD(kLdNoAlloc, "ld.global.L1::no_allocate")
+SWIGLU_DEFINE_LD(kLdNoAlloc256, "ld.global.L1::no_allocate.L2::256B")
+SWIGLU_DEFINE_LD(kLdNC, "ld.global.nc.L1::no_allocate")
+SWIGLU_DEFINE_LD(kLdNC256, "ld.global.nc.L1::no_allocate.L2::256B")
+#undef SWIGLU_DEFINE_LD
+
+#define SWIGLU_DEFINE_ST(KIND, QUAL)                                                           \
+    template <>                                                                                \
+    struct St<32, KIND> {                                                                      \
+        static __device__ __forceinline__ void run(void *p, const uint32_t *w) {               \
+            asm volatile(QUAL ".v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),       \
+                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),       \
+                         "r"(w[6]), "r"(w[7]));                                                 \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct St<16, KIND> {                                                                      \
+        static __device__ __forceinline__ void run(void *p, const uint32_t *w) {               \
+            asm volatile(QUAL ".v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]), \
+                         "r"(w[2]), "r"(w[3]));                                                 \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct St<8, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(void *p, const uint32_t *w) {               \
+            asm volatile(QUAL ".v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1]));        \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct St<4, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(void *p, const uint32_t *w) {               \
+            asm volatile(QUAL ".b32 [%0], %1;" ::"l"(p), "r"(w[0]));                            \
+        }                                                                                      \
+    };                                                                                         \
+    template <>                                                                                \
+    struct St<2, KIND> {                                                                       \
+        static __device__ __forceinline__ void run(void *p, const uint32_t *w) {               \
+            asm volatile(QUAL ".b16 [%0], %1;" ::"l"(p), "h"((unsigned short)w[0]));            \
+        }                                                                                      \
+    };
+
+SWIGLU_DEFINE_ST(kStStream, "st.global.cs")
+SWIGLU_DEFINE_ST(kStNoAlloc, "st.global.L1::no_allocate")
+SWIGLU_DEFINE_ST(kStPlain, "st.global")
+#undef SWIGLU_DEFINE_ST
 
 // ------------------------------------------------------------ data types ---
 // Element i of a pack <-> fp32.  Storage rounding is round-to-nearest-even.
@@ -81,11 +145,17 @@ struct F32 {
     // fp32 results below the 1e-7 absolute floor are never graded, so the
     // deep negative tail needs no rescaling (see BF16::kDeepScale).
     static constexpr bool kDeepScale = false;
+    // accurate expf and IEEE reciprocal: the fp32 tolerance needs them
+    static constexpr bool kFastExp = false;
     static __device__ __forceinline__ float get(const uint32_t *w, int i) {
         return __uint_as_float(w[i]);
     }
     static __device__ __forceinline__ void put(uint32_t *w, int i, float f) {
         w[i] = __float_as_uint(f);
+    }
+    static __device__ __forceinline__ void put2(uint32_t *w, int i, float f0, float f1) {
+        w[i] = __float_as_uint(f0);
+        w[i + 1] = __float_as_uint(f1);
     }
 };
 
@@ -100,6 +170,11 @@ struct BF16 {
     // is taken 64 binades higher and every result is scaled back by 2^-64 in
     // one final, correctly rounded multiply.
     static constexpr bool kDeepScale = true;
+    // The hardware base-2 exponential and reciprocal (relative errors near
+    // 2^-22) are far inside one bf16 step (2^-8).  With the deep-tail scaling
+    // above, the exponential's result is never subnormal where it matters, so
+    // their flush-to-zero of subnormal results is harmless.
+    static constexpr bool kFastExp = true;
     static __device__ __forceinline__ float get(const uint32_t *w, int i) {
         const uint32_t word = w[i >> 1];
         return __uint_as_float((i & 1) ? (word & 0xFFFF0000u) : (word << 16));
@@ -107,6 +182,11 @@ struct BF16 {
     static __device__ __forceinline__ void put(uint32_t *w, int i, float f) {
         const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(f));
         w[i >> 1] |= (i & 1) ? (b << 16) : b;
+    }
+    // elements i (even) and i + 1 in one packed conversion, both RNE
+    static __device__ __forceinline__ void put2(uint32_t *w, int i, float f0, float f1) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+        w[i >> 1] = (uint32_t)__bfloat16_as_ushort(h.x) | ((uint32_t)__bfloat16_as_ushort(h.y) << 16);
     }
 };
 
@@ -121,6 +201,20 @@ struct BF16 {
 
 constexpr float kLn2x64 = 44.3614195558365f;  // 64 ln 2
 constexpr float kTwoPowMinus64 = 5.421010862427522e-20f;  // 2^-64, exact
+constexpr float kLog2e = 1.4426950408889634f;
+
+// exp(x) = 2^(x log2 e) with the hardware base-2 exponential (PTX
+// ex2.approx.ftz), and the hardware reciprocal (PTX rcp.approx.ftz).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // silu'(g0 + d) near the root g0 of silu', as a Taylor polynomial in d.
 __device__ __forceinline__ float dsilu_near_root(float d) {
@@ -143,16 +237,17 @@ template <typename E, bool kGrad>
 __device__ __forceinline__ Act activation(float g) {
     const float a = fabsf(g);
     const bool pos = g >= 0.0f;
-    bool deep = false;
-    float arg = a;
-    if (E::kDeepScale) {
-        // for a > 64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or without
-        // the scaling and r = 1 stays exact
-        deep = !pos && a > 64.0f;
-        arg = deep ? __fsub_rn(a, kLn2x64) : a;
+    // deep: for g < -64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or
+    // without the scaling and r = 1 stays exact
+    const bool deep = E::kDeepScale && g < -64.0f;
+    float t;
+    if (E::kFastExp) {
+        // t = 2^(-|g| log2 e (+ 64 when deep))
+        t = ex2_approx(__fmaf_rn(a, -kLog2e, deep ? 64.0f : 0.0f));
+    } else {
+        t = expf(-(deep ? __fsub_rn(a, kLn2x64) : a));
     }
-    const float t = expf(-arg);
-    const float r = __frcp_rn(__fadd_rn(1.0f, t));
+    const float r = E::kFastExp ? rcp_approx(__fadd_rn(1.0f, t)) : __frcp_rn(__fadd_rn(1.0f, t));
     const float tr = __fmul_rn(t, r);
     const float s = pos ? r : tr;
     Act o;
@@ -168,6 +263,18 @@ __device__ __forceinline__ Act activation(float g) {
         }
     }
     return o;
+}
+
+// Round VEC fp32 results into the words of one pack (pairs at a time when
+// there are pairs).
+template <typename E, int VEC>
+__device__ __forceinline__ void store_pack(uint32_t *w, const float *v) {
+    if (VEC == 1) {
+        E::put(w, 0, v[0]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; i += 2) E::put2(w, i, v[i], v[i + 1]);
+    }
 }
 
 // ---------------------------------------------------------------- kernels ---
@@ -225,11 +332,12 @@ __device__ __forceinline__ void advance(int64_t step_q, int32_t step_r, int32_t 
     }
 }
 
-template <typename E, int VEC, int U>
+template <typename E, int VEC, int U, int LD, int ST>
 __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
-    using M = Mem<B>;
+    using L = Ld<B, LD>;
+    using S = St<B, ST>;
     const char *x = static_cast<const char *>(p.x);
     char *y = static_cast<char *>(p.y);
     const int64_t up_off = (int64_t)p.nvec * B;
@@ -243,33 +351,39 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
                 const char *px = x + (r[k] * p.x_stride + c[k]) * B;
-                M::load(px, g[k]);
-                M::load(px + up_off, u[k]);
+                L::run(px, g[k]);
+                L::run(px + up_off, u[k]);
             }
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
                 uint32_t o[NW] = {};
+                float yv[VEC];
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
                     const Act act = activation<E, false>(E::get(g[k], i));
-                    E::put(o, i, __fmul_rn(__fmul_rn(act.silu, E::get(u[k], i)), act.scale));
+                    yv[i] = __fmul_rn(__fmul_rn(act.silu, E::get(u[k], i)), act.scale);
                 }
-                M::store(y + (r[k] * p.y_stride + c[k]) * B, o);
+                store_pack<E, VEC>(o, yv);
+                S::run(y + (r[k] * p.y_stride + c[k]) * B, o);
             }
         }
         advance<U>(p.step_q, p.step_r, p.nvec, r, c);
     }
 }
 
-// IN_PLACE selects nothing but the aliasing contract (dx == x); the arithmetic
-// is the same template body, so both instances give identical bits.
-template <typename E, int VEC, int U, bool IN_PLACE>
+// IN_PLACE selects nothing but the aliasing contract (dx == x, so LD must be
+// a coherent kind); the arithmetic is the same template body, so both
+// instances give identical bits.
+template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
 __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p) {
+    static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256),
+                  "the in-place backward writes what it reads: no read-only loads");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
-    using M = Mem<B>;
+    using L = Ld<B, LD>;
+    using S = St<B, ST>;
     const char *dy = static_cast<const char *>(p.dy);
     const char *x = static_cast<const char *>(p.x);
     char *dx = IN_PLACE ? const_cast<char *>(x) : static_cast<char *>(p.dx);
@@ -284,27 +398,30 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
                 const char *px = x + (r[k] * p.x_stride + c[k]) * B;
-                M::load(dy + (r[k] * p.dy_stride + c[k]) * B, d[k]);
-                M::load(px, g[k]);
-                M::load(px + up_off, u[k]);
+                L::run(dy + (r[k] * p.dy_stride + c[k]) * B, d[k]);
+                L::run(px, g[k]);
+                L::run(px + up_off, u[k]);
             }
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
                 uint32_t og[NW] = {}, ou[NW] = {};
+                float gv[VEC], uv[VEC];
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
                     const float gf = E::get(g[k], i);
                     const float uf = E::get(u[k], i);
                     const float df = E::get(d[k], i);
                     const Act act = activation<E, true>(gf);
-                    E::put(og, i, __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale));
-                    E::put(ou, i, __fmul_rn(__fmul_rn(df, act.silu), act.scale));
+                    gv[i] = __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale);
+                    uv[i] = __fmul_rn(__fmul_rn(df, act.silu), act.scale);
                 }
+                store_pack<E, VEC>(og, gv);
+                store_pack<E, VEC>(ou, uv);
                 char *pdx = dx + (r[k] * p.dx_stride + c[k]) * B;
-                M::store(pdx, og);
-                M::store(pdx + up_off, ou);
+                S::run(pdx, og);
+                S::run(pdx + up_off, ou);
             }
         }
         advance<U>(p.step_q, p.step_r, p.nvec, r, c);
