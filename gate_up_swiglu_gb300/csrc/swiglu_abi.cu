@@ -51,10 +51,11 @@ bool span_of(const void *p, int64_t rows, int64_t cols, int64_t stride, int eb, 
 
 bool overlaps(const Span &a, const Span &b) { return a.lo < b.hi && b.lo < a.hi; }
 
-// Widest pack (32, 16, 8, 4 or 2 bytes) that divides n, every row stride and
-// every base address; returns the number of elements per pack.
-int pick_vec(int eb, int64_t n, const int64_t *strides, int ns, const void *const *ptrs, int np) {
-    for (int bytes = 32; bytes > eb; bytes /= 2) {
+// Widest pack (at most max_bytes: 32, 16, 8, 4 or 2 bytes) that divides n,
+// every row stride and every base address; returns the elements per pack.
+int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
+             const void *const *ptrs, int np) {
+    for (int bytes = max_bytes; bytes > eb; bytes /= 2) {
         const int vec = bytes / eb;
         bool ok = (n % vec) == 0;
         for (int i = 0; ok && i < ns; ++i) ok = (strides[i] % vec) == 0;
@@ -64,9 +65,20 @@ int pick_vec(int eb, int64_t n, const int64_t *strides, int ns, const void *cons
     return 1;
 }
 
+// Launch policy, chosen by sweeping pack width, unroll and resident CTAs per
+// SM over the Megatron-shape, large-FFN and Llama-like bf16 workloads on a
+// GB300: the forward is fastest with one 32-byte pack per operand in flight
+// and 4 CTAs of 256 threads per SM, both backward forms with two 16-byte packs
+// and 3 CTAs per SM.  Filling the SM with more CTAs lost 5-10 %.
+struct Policy {
+    int max_pack_bytes;
+    int max_ctas_per_sm;
+};
+constexpr Policy kFwdPolicy = {32, 4};
+constexpr Policy kBwdPolicy = {16, 3};
+
 // Packs in flight per operand per thread: one 32-byte pack, two 16-byte
-// packs, four 8-byte packs, else eight (measured on GB300: more unrolling of
-// 32-byte packs costs occupancy and loses).
+// packs, four 8-byte packs, else eight.
 constexpr int unroll_for(int pack_bytes) {
     return pack_bytes >= 32 ? 1 : (pack_bytes >= 16 ? 2 : (pack_bytes >= 8 ? 4 : 8));
 }
@@ -137,6 +149,7 @@ swiglu_status_t launch_fwd(const void *x, void *y, int64_t rows, int64_t n, int6
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm > kFwdPolicy.max_ctas_per_sm) per_sm = kFwdPolicy.max_ctas_per_sm;
     const int64_t nvec = n / VEC;
     const int64_t grid = grid_for<U>(rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -167,6 +180,7 @@ swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm > kBwdPolicy.max_ctas_per_sm) per_sm = kBwdPolicy.max_ctas_per_sm;
     const int64_t nvec = n / VEC;
     const int64_t grid = grid_for<U>(rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -186,32 +200,29 @@ swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
+// pick_vec never returns more than max_pack_bytes / kBytes elements, so only
+// those pack widths are instantiated.
 template <typename E>
 swiglu_status_t dispatch_fwd(int vec, const void *x, void *y, int64_t rows, int64_t n, int64_t sx,
                              int64_t sy, cudaStream_t st) {
-    switch (vec) {
-        case 16: if constexpr (E::kBytes == 2) return launch_fwd<E, 16>(x, y, rows, n, sx, sy, st); break;
-        case 8: return launch_fwd<E, 8>(x, y, rows, n, sx, sy, st);
-        case 4: return launch_fwd<E, 4>(x, y, rows, n, sx, sy, st);
-        case 2: return launch_fwd<E, 2>(x, y, rows, n, sx, sy, st);
-        default: break;
-    }
+    constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
+    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd<E, 16>(x, y, rows, n, sx, sy, st);
+    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd<E, 8>(x, y, rows, n, sx, sy, st);
+    if (vec == 4) return launch_fwd<E, 4>(x, y, rows, n, sx, sy, st);
+    if (vec == 2) return launch_fwd<E, 2>(x, y, rows, n, sx, sy, st);
     return launch_fwd<E, 1>(x, y, rows, n, sx, sy, st);
 }
 
 template <typename E, bool IP>
 swiglu_status_t dispatch_bwd(int vec, const void *dy, const void *x, void *dx, int64_t rows,
                              int64_t n, int64_t sdy, int64_t sx, int64_t sdx, cudaStream_t st) {
-    switch (vec) {
-        case 16:
-            if constexpr (E::kBytes == 2)
-                return launch_bwd<E, 16, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-            break;
-        case 8: return launch_bwd<E, 8, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-        case 4: return launch_bwd<E, 4, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-        case 2: return launch_bwd<E, 2, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-        default: break;
-    }
+    constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;
+    if constexpr (kMaxVec >= 16)
+        if (vec == 16) return launch_bwd<E, 16, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
+    if constexpr (kMaxVec >= 8)
+        if (vec == 8) return launch_bwd<E, 8, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
+    if (vec == 4) return launch_bwd<E, 4, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
+    if (vec == 2) return launch_bwd<E, 2, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
     return launch_bwd<E, 1, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
 }
 
@@ -242,7 +253,7 @@ swiglu_status_t swiglu_gateup_fwd(const void *x, void *y, int64_t rows, int64_t 
 
     const int64_t strides[2] = {x_row_stride, y_row_stride};
     const void *ptrs[2] = {x, y};
-    const int vec = pick_vec(eb, n, strides, 2, ptrs, 2);
+    const int vec = pick_vec(eb, kFwdPolicy.max_pack_bytes, n, strides, 2, ptrs, 2);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWIGLU_F32)
         return dispatch_fwd<swiglu::F32>(vec, x, y, rows, n, x_row_stride, y_row_stride, s);
@@ -279,7 +290,7 @@ swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64
 
     const int64_t strides[3] = {dy_row_stride, x_row_stride, dx_row_stride};
     const void *ptrs[3] = {dy, x, dx};
-    const int vec = pick_vec(eb, n, strides, 3, ptrs, 3);
+    const int vec = pick_vec(eb, kBwdPolicy.max_pack_bytes, n, strides, 3, ptrs, 3);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWIGLU_F32) {
         if (in_place)

@@ -166,16 +166,19 @@ def test_golden_special_values(sw):
 SENTINEL_F32 = -12345.5
 CASES = [
     # (dtype, rows, n, x_pad, y_pad, dy_pad, dx_pad, misalign_elems)
-    ("bf16", 37, 4096, 0, 0, 0, 0, 0),    # 16-byte packs
+    # pack widths: forward up to 32 bytes, backward up to 16 bytes
+    ("bf16", 37, 4096, 0, 0, 0, 0, 0),    # fwd 32-byte, bwd 16-byte packs
+    ("bf16", 37, 4104, 0, 0, 0, 0, 0),    # 16-byte packs (n % 16 == 8)
     ("bf16", 37, 4100, 0, 0, 0, 0, 0),    # 8-byte packs (n % 8 == 4)
     ("bf16", 29, 4098, 0, 0, 0, 0, 0),    # 4-byte packs (n % 4 == 2)
     ("bf16", 31, 1001, 0, 0, 0, 0, 0),    # single elements (odd n)
-    ("bf16", 23, 2048, 8, 16, 8, 24, 0),  # padded strides keep 16-byte packs
+    ("bf16", 23, 2048, 16, 32, 16, 32, 0),  # padded strides keep 32-byte packs
+    ("bf16", 23, 2048, 8, 16, 8, 24, 0),  # padding drops the forward to 16 bytes
     ("bf16", 23, 2048, 2, 6, 2, 4, 0),    # padding drops to 4-byte packs
     ("bf16", 19, 2048, 0, 0, 0, 0, 1),    # misaligned base pointers
     ("bf16", 3000, 8, 0, 0, 0, 0, 0),     # many short rows (grid-stride, row carry)
     ("bf16", 5, 1, 0, 0, 0, 0, 0),        # n = 1
-    ("f32", 37, 4096, 0, 0, 0, 0, 0),     # 16-byte packs
+    ("f32", 37, 4096, 0, 0, 0, 0, 0),     # fwd 32-byte, bwd 16-byte packs
     ("f32", 37, 4098, 0, 0, 0, 0, 0),     # 8-byte packs
     ("f32", 31, 5503, 0, 0, 0, 0, 0),     # odd n
     ("f32", 23, 1024, 4, 12, 4, 8, 0),    # padded strides, 16-byte packs
