@@ -1,0 +1,122 @@
+"""Autograd function and Megatron-style module over the libswiglu C ABI.
+
+The user-facing layer of the Liger-Kernel Megatron SwiGLU page:
+``GateUpSwiGLUFunction`` plays the part of its fused gate-up autograd function
+(§What's added) and ``GateUpSwiGLU`` the part of its Megatron module: the
+positional signature of Megatron's ``bias_swiglu_impl`` (§How to use, Mode 2),
+the opt-in ``in_place`` backward (§Optional in_place=True), the delegation of
+unsupported Megatron features to a fallback that is logged once, or an error
+when no fallback is given (§Scope), and the guard against a second backward
+after an in-place one (§Known issues 1).
+
+All arithmetic runs in the CUDA kernels; this module only decides what to call.
+"""
+from __future__ import annotations
+
+import logging
+from typing import Callable, Optional
+
+import torch
+
+from . import swiglu_gateup_bwd, swiglu_gateup_fwd
+
+log = logging.getLogger(__name__)
+
+
+def _bump_version(t: torch.Tensor) -> None:
+    # the kernel writes through a raw pointer, which autograd cannot see
+    inc = getattr(torch.autograd.graph, "increment_version", None)
+    if inc is not None:
+        inc(t)
+
+
+class GateUpSwiGLUFunction(torch.autograd.Function):
+    """y = silu(x[..., :n]) * x[..., n:] with the fused backward.
+
+    ``in_place=True`` makes the backward write the gradient over the saved fc1
+    buffer ``x`` and return that buffer as the input gradient: no extra
+    ``[..., 2n]`` allocation, and ``x`` is destroyed.  Running the backward a
+    second time over the same graph (``retain_graph=True``) then raises instead
+    of silently producing garbage.
+    """
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, in_place: bool = False):
+        y = swiglu_gateup_fwd(x)
+        ctx.save_for_backward(x)
+        ctx.in_place = bool(in_place)
+        ctx.already_backward = False
+        return y
+
+    @staticmethod
+    def backward(ctx, dy: torch.Tensor):
+        # checked before the saved buffer is unpacked: after an in-place backward
+        # autograd's own version check would fire with a less specific message
+        if ctx.in_place:
+            if ctx.already_backward:
+                raise RuntimeError(
+                    "GateUpSwiGLUFunction: backward already ran with in_place=True, which "
+                    "overwrote the saved fc1 buffer; a second backward (retain_graph=True) "
+                    "would compute garbage")
+            ctx.already_backward = True
+        (x,) = ctx.saved_tensors
+        dy = dy.contiguous()
+        if ctx.in_place:
+            dx = swiglu_gateup_bwd(dy, x, in_place=True)
+            _bump_version(x)
+        else:
+            dx = swiglu_gateup_bwd(dy, x)
+        return dx, None
+
+
+def gate_up_swiglu(x: torch.Tensor, in_place: bool = False) -> torch.Tensor:
+    return GateUpSwiGLUFunction.apply(x, in_place)
+
+
+class GateUpSwiGLU(torch.nn.Module):
+    """Drop-in for Megatron's ``bias_swiglu_impl(intermediate, bias,
+    fp8_input_store, cpu_offload_input)``.
+
+    Supported: ``bias=None``, fp32 or bf16, 2D ``[tokens, 2n]`` or 3D
+    ``[s, b, 2n]`` CUDA tensors.  A call that needs a feature the kernels do
+    not have (a bias, fp8 input storage, cpu offload of the input) goes to
+    ``fallback_impl`` (logged once per reason); with ``fallback_impl=None`` it
+    raises ``NotImplementedError``.
+    """
+
+    def __init__(self, in_place: bool = False,
+                 fallback_impl: Optional[Callable] = None):
+        super().__init__()
+        self.in_place = in_place
+        self.fallback_impl = fallback_impl
+        self._logged = set()
+
+    def _unsupported(self, bias, fp8_input_store, cpu_offload_input) -> Optional[str]:
+        if bias is not None:
+            return "bias is not None"
+        if fp8_input_store:
+            return "fp8_input_store=True"
+        if cpu_offload_input:
+            return "cpu_offload_input=True"
+        return None
+
+    def forward(self, intermediate: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                fp8_input_store: bool = False, cpu_offload_input: bool = False) -> torch.Tensor:
+        reason = self._unsupported(bias, fp8_input_store, cpu_offload_input)
+        if reason is not None:
+            if self.fallback_impl is None:
+                raise NotImplementedError(f"GateUpSwiGLU: {reason} is not supported by the fused "
+                                          "kernels and no fallback_impl was given")
+            if reason not in self._logged:
+                self._logged.add(reason)
+                log.warning("GateUpSwiGLU: %s; delegating to the fallback implementation", reason)
+            return self.fallback_impl(intermediate, bias, fp8_input_store, cpu_offload_input)
+        if intermediate.dim() not in (2, 3):
+            raise ValueError(f"GateUpSwiGLU: expected a 2D [tokens, 2n] or 3D [s, b, 2n] input, "
+                             f"got shape {tuple(intermediate.shape)}")
+        if intermediate.shape[-1] % 2:
+            raise ValueError("GateUpSwiGLU: the last dimension (2n) must be even")
+        if intermediate.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError(f"GateUpSwiGLU: dtype {intermediate.dtype} is not supported "
+                             "(float32 or bfloat16)")
+        return GateUpSwiGLUFunction.apply(intermediate, self.in_place)
