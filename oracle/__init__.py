@@ -62,6 +62,11 @@ def load(path: str = None):
         lib.oracle_swiglu_fwd.restype = ctypes.c_int
         lib.oracle_swiglu_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int]
         lib.oracle_swiglu_bwd.restype = ctypes.c_int
+        lib.oracle_silu_mul_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_silu_mul_fwd.restype = ctypes.c_int
+        lib.oracle_silu_mul_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
+                                            ctypes.c_int]
+        lib.oracle_silu_mul_bwd.restype = ctypes.c_int
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         if path is None:
@@ -107,6 +112,38 @@ def bwd(dy: torch.Tensor, x: torch.Tensor, dx: torch.Tensor = None, lib=None) ->
     if rc != 0:
         raise ValueError("oracle_swiglu_bwd rejected its arguments")
     return dx
+
+
+def silu_mul_fwd(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor = None, lib=None) -> torch.Tensor:
+    """Two-tensor form: c = silu(a) * b, rounded once to a's dtype."""
+    lib = lib or load()
+    for t, nm in ((a, "a"), (b, "b")):
+        _rowmajor(t, nm)
+    rows, n = a.shape
+    if c is None:
+        c = torch.empty((rows, n), dtype=a.dtype)
+    _rowmajor(c, "c")
+    rc = lib.oracle_silu_mul_fwd(a.data_ptr(), b.data_ptr(), c.data_ptr(), rows, n, a.stride(0),
+                                 b.stride(0), c.stride(0), _CODE[a.dtype])
+    if rc != 0:
+        raise ValueError("oracle_silu_mul_fwd rejected its arguments")
+    return c
+
+
+def silu_mul_bwd(dc, a, b, da=None, db=None, lib=None):
+    """Two-tensor form: returns (da, db); pass da=a, db=b for the in-place form."""
+    lib = lib or load()
+    for t, nm in ((dc, "dc"), (a, "a"), (b, "b")):
+        _rowmajor(t, nm)
+    rows, n = a.shape
+    da = torch.empty((rows, n), dtype=a.dtype) if da is None else da
+    db = torch.empty((rows, n), dtype=a.dtype) if db is None else db
+    rc = lib.oracle_silu_mul_bwd(dc.data_ptr(), a.data_ptr(), b.data_ptr(), da.data_ptr(),
+                                 db.data_ptr(), rows, n, dc.stride(0), a.stride(0), b.stride(0),
+                                 da.stride(0), db.stride(0), _CODE[a.dtype])
+    if rc != 0:
+        raise ValueError("oracle_silu_mul_bwd rejected its arguments")
+    return da, db
 
 
 def bf16_from_double(v: float, lib=None) -> int:

@@ -161,3 +161,41 @@ int oracle_swiglu_bwd(const void *dy, const void *x, void *dx, int64_t rows, int
     }
     return ORACLE_OK;
 }
+
+/* ---- the two-tensor formulation ------------------------------------------- */
+/* Liger-Kernel Megatron SwiGLU page, §Background: Liger's earlier SwiGLU takes
+ * the gate a and the up projection b as two separate tensors, as HuggingFace
+ * models produce them.  Same arithmetic, separate buffers:
+ *   c[r, j] = silu(a[r, j]) * b[r, j]
+ *   da[r, j] = dc * b * s * (1 + a (1 - s)),   db[r, j] = dc * a * s.
+ * da may be a and db may be b (each pair is read before it is written). */
+int oracle_silu_mul_fwd(const void *a, const void *b, void *c, int64_t rows, int64_t n,
+                        int64_t sa, int64_t sb, int64_t sc, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double g = load_elem(a, r * sa + j, dtype);
+            double u = load_elem(b, r * sb + j, dtype);
+            store_elem(c, r * sc + j, dtype, swiglu_fwd_pair(g, u));
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_silu_mul_bwd(const void *dc, const void *a, const void *b, void *da, void *db,
+                        int64_t rows, int64_t n, int64_t sdc, int64_t sa, int64_t sb,
+                        int64_t sda, int64_t sdb, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double d = load_elem(dc, r * sdc + j, dtype);
+            double g = load_elem(a, r * sa + j, dtype);
+            double u = load_elem(b, r * sb + j, dtype);
+            double dg, du;
+            swiglu_bwd_pair(d, g, u, &dg, &du);
+            store_elem(da, r * sda + j, dtype, dg);
+            store_elem(db, r * sdb + j, dtype, du);
+        }
+    }
+    return ORACLE_OK;
+}

@@ -276,9 +276,38 @@ def pin_strided_layouts(lib):
     assert torch.equal(xi[:, :2 * n], dx) and torch.all(torch.isnan(xi[:, 2 * n:]))
 
 
+def pin_two_tensor_form(lib):
+    """The two-tensor entry points equal torch float64 autograd of
+    F.silu(a) * b on separately strided buffers, and equal the fused form on
+    the halves of one buffer."""
+    for seed, (rows, n) in enumerate([(13, 29), (4, 1), (3, 257)]):
+        a = _rand((rows, n + 3), 70 + seed, 4.0)[:, :n]
+        b = _rand((rows, n + 5), 80 + seed, 2.0)[:, :n]
+        dc = _rand((rows, n), 90 + seed)
+        at, bt = a.clone().requires_grad_(True), b.clone().requires_grad_(True)
+        ref = F.silu(at) * bt
+        ref.backward(dc)
+        c = oracle.silu_mul_fwd(a, b, torch.empty(rows, n + 4, dtype=F64)[:, :n], lib=lib)
+        da, db = oracle.silu_mul_bwd(dc, a, b, torch.empty(rows, n + 2, dtype=F64)[:, :n],
+                                     torch.empty(rows, n + 7, dtype=F64)[:, :n], lib=lib)
+        assert torch.allclose(c, ref.detach(), rtol=1e-13, atol=1e-300)
+        assert torch.allclose(da, at.grad, rtol=1e-12, atol=1e-14)
+        assert torch.allclose(db, bt.grad, rtol=1e-13, atol=1e-300)
+        x = torch.cat([a, b], dim=1).float()
+        dcf = dc.float()
+        af, bf = x[:, :n].contiguous(), x[:, n:].contiguous()
+        assert torch.equal(oracle.silu_mul_fwd(af, bf, lib=lib), oracle.fwd(x, lib=lib))
+        da2, db2 = oracle.silu_mul_bwd(dcf, af, bf, lib=lib)
+        assert torch.equal(torch.cat([da2, db2], 1), oracle.bwd(dcf, x, lib=lib))
+        # in place over a and b
+        ai, bi = af.clone(), bf.clone()
+        oracle.silu_mul_bwd(dcf, ai, bi, ai, bi, lib=lib)
+        assert torch.equal(ai, da2) and torch.equal(bi, db2)
+
+
 PINS = [pin_zero_gate, pin_saturation, pin_stationary_point, pin_finite_differences,
         pin_torch_two_tensor, pin_bf16_rounding_brute, pin_rounding_matches_torch,
-        pin_bf16_all_gates, pin_strided_layouts]
+        pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -311,6 +340,9 @@ MUTATIONS = {
     "f32_truncates": ("float f = (float)v; /* IEEE",
                       "float f = (float)v; if (fabs((double)f) > fabs(v)) f = nextafterf(f, 0.0f); /* IEEE"),
     "dy_stride_ignored": ("load_elem(dy, r * sdy + j", "load_elem(dy, r * n + j"),
+    "two_tensor_a_b_swapped": ("double g = load_elem(a, r * sa + j, dtype);\n            double u = load_elem(b, r * sb + j, dtype);\n            store_elem(c",
+                               "double g = load_elem(b, r * sb + j, dtype);\n            double u = load_elem(a, r * sa + j, dtype);\n            store_elem(c"),
+    "two_tensor_db_stride": ("store_elem(db, r * sdb + j", "store_elem(db, r * sda + j"),
 }
 
 
