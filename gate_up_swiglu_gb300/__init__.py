@@ -31,8 +31,8 @@ STATUS = {0: "SWIGLU_OK", -1: "SWIGLU_ERR_NULL", -2: "SWIGLU_ERR_DTYPE", -3: "SW
           -4: "SWIGLU_ERR_STRIDE", -5: "SWIGLU_ERR_ALIAS", -6: "SWIGLU_ERR_CUDA"}
 
 # every symbol include/swiglu.h declares
-EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_status_string",
-           "swiglu_last_cuda_error", "swiglu_abi_version")
+EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
+           "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
 
 
 class SwigluError(RuntimeError):
@@ -52,6 +52,10 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_gateup_fwd.restype = i32
     lib.swiglu_gateup_bwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
     lib.swiglu_gateup_bwd.restype = i32
+    lib.swiglu_silu_mul_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp]
+    lib.swiglu_silu_mul_fwd.restype = i32
+    lib.swiglu_silu_mul_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, vp]
+    lib.swiglu_silu_mul_bwd.restype = i32
     lib.swiglu_status_string.argtypes = [i32]
     lib.swiglu_status_string.restype = ctypes.c_char_p
     lib.swiglu_last_cuda_error.argtypes = []
@@ -154,5 +158,45 @@ def swiglu_gateup_bwd(dy: torch.Tensor, x: torch.Tensor, dx: torch.Tensor = None
     return dx
 
 
-__all__ = ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "status_string", "SwigluError", "lib",
+def swiglu_silu_mul_fwd(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor = None,
+                        stream=None) -> torch.Tensor:
+    """Two-tensor form: c = silu(a) * b for [..., n] tensors a, b."""
+    if c is None:
+        c = torch.empty(a.shape, dtype=a.dtype, device=a.device)
+    _check_cuda(a, b, c)
+    rows, n, sa = _rows_view(a, "a")
+    (rb, nb, sb), (rc, nc, sc) = _rows_view(b, "b"), _rows_view(c, "c")
+    if (rb, nb) != (rows, n) or (rc, nc) != (rows, n):
+        raise ValueError("a, b and c must have the same [..., n] shape")
+    with torch.cuda.device(a.device):
+        st = lib.swiglu_silu_mul_fwd(a.data_ptr(), b.data_ptr(), c.data_ptr(), rows, n, sa, sb, sc,
+                                     _DTYPE[a.dtype], _stream_handle(a, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_silu_mul_fwd")
+    return c
+
+
+def swiglu_silu_mul_bwd(dc: torch.Tensor, a: torch.Tensor, b: torch.Tensor, da=None, db=None,
+                        in_place: bool = False, stream=None):
+    """Two-tensor form: returns (da, db).  ``in_place=True`` writes da over a
+    and db over b."""
+    if in_place:
+        da, db = a, b
+    da = torch.empty(a.shape, dtype=a.dtype, device=a.device) if da is None else da
+    db = torch.empty(b.shape, dtype=b.dtype, device=b.device) if db is None else db
+    _check_cuda(dc, a, b, da, db)
+    views = [_rows_view(t, nm) for t, nm in ((dc, "dc"), (a, "a"), (b, "b"), (da, "da"), (db, "db"))]
+    rows, n = views[1][0], views[1][1]
+    if any((v[0], v[1]) != (rows, n) for v in views):
+        raise ValueError("dc, a, b, da and db must have the same [..., n] shape")
+    with torch.cuda.device(a.device):
+        st = lib.swiglu_silu_mul_bwd(dc.data_ptr(), a.data_ptr(), b.data_ptr(), da.data_ptr(),
+                                     db.data_ptr(), rows, n, *[v[2] for v in views],
+                                     _DTYPE[a.dtype], _stream_handle(a, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_silu_mul_bwd")
+    return da, db
+
+
+__all__ = ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd", "status_string", "SwigluError", "lib",
            "SWIGLU_F32", "SWIGLU_BF16", "EXPORTS", "LIB_PATH"]

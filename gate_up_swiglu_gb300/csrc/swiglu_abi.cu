@@ -137,9 +137,24 @@ int64_t grid_for(int64_t total_packs, const Device &d, int per_sm) {
     return need < full ? need : full;
 }
 
+// One operand of a launch: base pointer and row stride in elements.
+struct Operand {
+    const void *p;
+    int64_t stride;
+};
+
+struct FwdArgs {
+    Operand g, u, y;
+    int64_t rows, n;
+};
+
+struct BwdArgs {
+    Operand dy, g, u, dg, du;
+    int64_t rows, n;
+};
+
 template <typename E, int VEC>
-swiglu_status_t launch_fwd(const void *x, void *y, int64_t rows, int64_t n, int64_t sx,
-                           int64_t sy, cudaStream_t stream) {
+swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
     auto kernel = swiglu::swiglu_fwd_kernel<E, VEC, U, kLoadOutOfPlace, kStore>;
@@ -150,15 +165,17 @@ swiglu_status_t launch_fwd(const void *x, void *y, int64_t rows, int64_t n, int6
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
     if (per_sm > kFwdPolicy.max_ctas_per_sm) per_sm = kFwdPolicy.max_ctas_per_sm;
-    const int64_t nvec = n / VEC;
-    const int64_t grid = grid_for<U>(rows * nvec, d, per_sm);
+    const int64_t nvec = a.n / VEC;
+    const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
     swiglu::FwdParams p;
-    p.x = x;
-    p.y = y;
-    p.rows = rows;
-    p.x_stride = sx / VEC;
-    p.y_stride = sy / VEC;
+    p.g = a.g.p;
+    p.u = a.u.p;
+    p.y = const_cast<void *>(a.y.p);
+    p.rows = a.rows;
+    p.g_stride = a.g.stride / VEC;
+    p.u_stride = a.u.stride / VEC;
+    p.y_stride = a.y.stride / VEC;
     p.step_q = step / nvec;
     p.nvec = (int32_t)nvec;
     p.step_r = (int32_t)(step % nvec);
@@ -168,8 +185,7 @@ swiglu_status_t launch_fwd(const void *x, void *y, int64_t rows, int64_t n, int6
 }
 
 template <typename E, int VEC, bool IN_PLACE>
-swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows, int64_t n,
-                           int64_t sdy, int64_t sx, int64_t sdx, cudaStream_t stream) {
+swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
     auto kernel = swiglu::swiglu_bwd_kernel<E, VEC, U, IN_PLACE,
@@ -181,17 +197,21 @@ swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
     if (per_sm > kBwdPolicy.max_ctas_per_sm) per_sm = kBwdPolicy.max_ctas_per_sm;
-    const int64_t nvec = n / VEC;
-    const int64_t grid = grid_for<U>(rows * nvec, d, per_sm);
+    const int64_t nvec = a.n / VEC;
+    const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
     swiglu::BwdParams p;
-    p.dy = dy;
-    p.x = x;
-    p.dx = dx;
-    p.rows = rows;
-    p.dy_stride = sdy / VEC;
-    p.x_stride = sx / VEC;
-    p.dx_stride = sdx / VEC;
+    p.dy = a.dy.p;
+    p.g = a.g.p;
+    p.u = a.u.p;
+    p.dg = const_cast<void *>(a.dg.p);
+    p.du = const_cast<void *>(a.du.p);
+    p.rows = a.rows;
+    p.dy_stride = a.dy.stride / VEC;
+    p.g_stride = a.g.stride / VEC;
+    p.u_stride = a.u.stride / VEC;
+    p.dg_stride = a.dg.stride / VEC;
+    p.du_stride = a.du.stride / VEC;
     p.step_q = step / nvec;
     p.nvec = (int32_t)nvec;
     p.step_r = (int32_t)(step % nvec);
@@ -200,34 +220,51 @@ swiglu_status_t launch_bwd(const void *dy, const void *x, void *dx, int64_t rows
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
-// pick_vec never returns more than max_pack_bytes / kBytes elements, so only
-// those pack widths are instantiated.
+// The widest pack every operand allows (pick_vec never returns more than
+// max_pack_bytes / kBytes elements, so only those widths are instantiated).
 template <typename E>
-swiglu_status_t dispatch_fwd(int vec, const void *x, void *y, int64_t rows, int64_t n, int64_t sx,
-                             int64_t sy, cudaStream_t st) {
+swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
+    const int64_t strides[3] = {a.g.stride, a.u.stride, a.y.stride};
+    const void *ptrs[3] = {a.g.p, a.u.p, a.y.p};
+    const int vec = pick_vec(E::kBytes, kFwdPolicy.max_pack_bytes, a.n, strides, 3, ptrs, 3);
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
-    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd<E, 16>(x, y, rows, n, sx, sy, st);
-    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd<E, 8>(x, y, rows, n, sx, sy, st);
-    if (vec == 4) return launch_fwd<E, 4>(x, y, rows, n, sx, sy, st);
-    if (vec == 2) return launch_fwd<E, 2>(x, y, rows, n, sx, sy, st);
-    return launch_fwd<E, 1>(x, y, rows, n, sx, sy, st);
+    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd<E, 16>(a, st);
+    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd<E, 8>(a, st);
+    if (vec == 4) return launch_fwd<E, 4>(a, st);
+    if (vec == 2) return launch_fwd<E, 2>(a, st);
+    return launch_fwd<E, 1>(a, st);
 }
 
 template <typename E, bool IP>
-swiglu_status_t dispatch_bwd(int vec, const void *dy, const void *x, void *dx, int64_t rows,
-                             int64_t n, int64_t sdy, int64_t sx, int64_t sdx, cudaStream_t st) {
+swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
+    const int64_t strides[5] = {a.dy.stride, a.g.stride, a.u.stride, a.dg.stride, a.du.stride};
+    const void *ptrs[5] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p};
+    const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, 5);
     constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;
-    if constexpr (kMaxVec >= 16)
-        if (vec == 16) return launch_bwd<E, 16, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-    if constexpr (kMaxVec >= 8)
-        if (vec == 8) return launch_bwd<E, 8, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-    if (vec == 4) return launch_bwd<E, 4, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-    if (vec == 2) return launch_bwd<E, 2, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
-    return launch_bwd<E, 1, IP>(dy, x, dx, rows, n, sdy, sx, sdx, st);
+    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_bwd<E, 16, IP>(a, st);
+    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_bwd<E, 8, IP>(a, st);
+    if (vec == 4) return launch_bwd<E, 4, IP>(a, st);
+    if (vec == 2) return launch_bwd<E, 2, IP>(a, st);
+    return launch_bwd<E, 1, IP>(a, st);
 }
 
-// Checks shared by both directions: shape range and the int64 byte extents.
-swiglu_status_t check_shape(int64_t rows, int64_t n) {
+swiglu_status_t run_fwd(swiglu_dtype_t dtype, const FwdArgs &a, swiglu_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == SWIGLU_F32) return dispatch_fwd<swiglu::F32>(a, s);
+    return dispatch_fwd<swiglu::BF16>(a, s);
+}
+
+swiglu_status_t run_bwd(swiglu_dtype_t dtype, bool in_place, const BwdArgs &a,
+                        swiglu_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == SWIGLU_F32)
+        return in_place ? dispatch_bwd<swiglu::F32, true>(a, s) : dispatch_bwd<swiglu::F32, false>(a, s);
+    return in_place ? dispatch_bwd<swiglu::BF16, true>(a, s) : dispatch_bwd<swiglu::BF16, false>(a, s);
+}
+
+// Checks shared by every entry point: dtype and shape range.
+swiglu_status_t check_common(swiglu_dtype_t dtype, int64_t rows, int64_t n) {
+    if (elem_bytes(dtype) == 0) return SWIGLU_ERR_DTYPE;
     if (rows < 0 || n < 0 || n > SWIGLU_MAX_N) return SWIGLU_ERR_SHAPE;
     return SWIGLU_OK;
 }
@@ -239,36 +276,29 @@ extern "C" {
 swiglu_status_t swiglu_gateup_fwd(const void *x, void *y, int64_t rows, int64_t n,
                                   int64_t x_row_stride, int64_t y_row_stride,
                                   swiglu_dtype_t dtype, swiglu_stream_t stream) {
-    const int eb = elem_bytes(dtype);
-    if (eb == 0) return SWIGLU_ERR_DTYPE;
-    swiglu_status_t st = check_shape(rows, n);
+    swiglu_status_t st = check_common(dtype, rows, n);
     if (st != SWIGLU_OK) return st;
     if (rows == 0 || n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
     if (x == nullptr || y == nullptr) return SWIGLU_ERR_NULL;
     if (x_row_stride < 2 * n || y_row_stride < n) return SWIGLU_ERR_STRIDE;
     Span sxs, sys;
     if (!span_of(x, rows, 2 * n, x_row_stride, eb, sxs) || !span_of(y, rows, n, y_row_stride, eb, sys))
         return SWIGLU_ERR_SHAPE;
     if (overlaps(sxs, sys)) return SWIGLU_ERR_ALIAS;
-
-    const int64_t strides[2] = {x_row_stride, y_row_stride};
-    const void *ptrs[2] = {x, y};
-    const int vec = pick_vec(eb, kFwdPolicy.max_pack_bytes, n, strides, 2, ptrs, 2);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype == SWIGLU_F32)
-        return dispatch_fwd<swiglu::F32>(vec, x, y, rows, n, x_row_stride, y_row_stride, s);
-    return dispatch_fwd<swiglu::BF16>(vec, x, y, rows, n, x_row_stride, y_row_stride, s);
+    const char *xb = static_cast<const char *>(x);
+    FwdArgs a{{x, x_row_stride}, {xb + n * eb, x_row_stride}, {y, y_row_stride}, rows, n};
+    return run_fwd(dtype, a, stream);
 }
 
 swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64_t rows,
                                   int64_t n, int64_t dy_row_stride, int64_t x_row_stride,
                                   int64_t dx_row_stride, swiglu_dtype_t dtype, int in_place,
                                   swiglu_stream_t stream) {
-    const int eb = elem_bytes(dtype);
-    if (eb == 0) return SWIGLU_ERR_DTYPE;
-    swiglu_status_t st = check_shape(rows, n);
+    swiglu_status_t st = check_common(dtype, rows, n);
     if (st != SWIGLU_OK) return st;
     if (rows == 0 || n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
     if (in_place) {
         if (dx == nullptr) dx = const_cast<void *>(x);
         if (dx_row_stride == 0) dx_row_stride = x_row_stride;
@@ -287,23 +317,69 @@ swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64
     } else {
         if (overlaps(sdxs, sxs) || overlaps(sdxs, sdys)) return SWIGLU_ERR_ALIAS;
     }
+    const char *xb = static_cast<const char *>(x);
+    char *dxb = static_cast<char *>(dx);
+    BwdArgs a{{dy, dy_row_stride},
+              {x, x_row_stride},
+              {xb + n * eb, x_row_stride},
+              {dx, dx_row_stride},
+              {dxb + n * eb, dx_row_stride},
+              rows,
+              n};
+    return run_bwd(dtype, in_place != 0, a, stream);
+}
 
-    const int64_t strides[3] = {dy_row_stride, x_row_stride, dx_row_stride};
-    const void *ptrs[3] = {dy, x, dx};
-    const int vec = pick_vec(eb, kBwdPolicy.max_pack_bytes, n, strides, 3, ptrs, 3);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype == SWIGLU_F32) {
-        if (in_place)
-            return dispatch_bwd<swiglu::F32, true>(vec, dy, x, dx, rows, n, dy_row_stride,
-                                                   x_row_stride, dx_row_stride, s);
-        return dispatch_bwd<swiglu::F32, false>(vec, dy, x, dx, rows, n, dy_row_stride,
-                                                x_row_stride, dx_row_stride, s);
-    }
-    if (in_place)
-        return dispatch_bwd<swiglu::BF16, true>(vec, dy, x, dx, rows, n, dy_row_stride,
-                                                x_row_stride, dx_row_stride, s);
-    return dispatch_bwd<swiglu::BF16, false>(vec, dy, x, dx, rows, n, dy_row_stride, x_row_stride,
-                                             dx_row_stride, s);
+swiglu_status_t swiglu_silu_mul_fwd(const void *a, const void *b, void *c, int64_t rows, int64_t n,
+                                    int64_t a_row_stride, int64_t b_row_stride,
+                                    int64_t c_row_stride, swiglu_dtype_t dtype,
+                                    swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
+    if (a == nullptr || b == nullptr || c == nullptr) return SWIGLU_ERR_NULL;
+    if (a_row_stride < n || b_row_stride < n || c_row_stride < n) return SWIGLU_ERR_STRIDE;
+    Span sa, sb, sc;
+    if (!span_of(a, rows, n, a_row_stride, eb, sa) || !span_of(b, rows, n, b_row_stride, eb, sb) ||
+        !span_of(c, rows, n, c_row_stride, eb, sc))
+        return SWIGLU_ERR_SHAPE;
+    if (overlaps(sc, sa) || overlaps(sc, sb)) return SWIGLU_ERR_ALIAS;
+    FwdArgs args{{a, a_row_stride}, {b, b_row_stride}, {c, c_row_stride}, rows, n};
+    return run_fwd(dtype, args, stream);
+}
+
+swiglu_status_t swiglu_silu_mul_bwd(const void *dc, const void *a, const void *b, void *da,
+                                    void *db, int64_t rows, int64_t n, int64_t dc_row_stride,
+                                    int64_t a_row_stride, int64_t b_row_stride,
+                                    int64_t da_row_stride, int64_t db_row_stride,
+                                    swiglu_dtype_t dtype, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
+    if (dc == nullptr || a == nullptr || b == nullptr || da == nullptr || db == nullptr)
+        return SWIGLU_ERR_NULL;
+    if (dc_row_stride < n || a_row_stride < n || b_row_stride < n || da_row_stride < n ||
+        db_row_stride < n)
+        return SWIGLU_ERR_STRIDE;
+    Span sdc, sa, sb, sda, sdb;
+    if (!span_of(dc, rows, n, dc_row_stride, eb, sdc) || !span_of(a, rows, n, a_row_stride, eb, sa) ||
+        !span_of(b, rows, n, b_row_stride, eb, sb) ||
+        !span_of(da, rows, n, da_row_stride, eb, sda) ||
+        !span_of(db, rows, n, db_row_stride, eb, sdb))
+        return SWIGLU_ERR_SHAPE;
+    // an output may be exactly its own input (same pointer and stride);
+    // otherwise it may overlap no input and not the other output
+    const bool da_is_a = da == a && da_row_stride == a_row_stride;
+    const bool db_is_b = db == b && db_row_stride == b_row_stride;
+    if (overlaps(sda, sdb)) return SWIGLU_ERR_ALIAS;
+    if (overlaps(sda, sdc) || overlaps(sda, sb) || (!da_is_a && overlaps(sda, sa)))
+        return SWIGLU_ERR_ALIAS;
+    if (overlaps(sdb, sdc) || overlaps(sdb, sa) || (!db_is_b && overlaps(sdb, sb)))
+        return SWIGLU_ERR_ALIAS;
+    BwdArgs args{{dc, dc_row_stride}, {a, a_row_stride},   {b, b_row_stride},
+                 {da, da_row_stride}, {db, db_row_stride}, rows, n};
+    return run_bwd(dtype, da_is_a || db_is_b, args, stream);
 }
 
 const char *swiglu_status_string(swiglu_status_t status) {
@@ -321,6 +397,6 @@ const char *swiglu_status_string(swiglu_status_t status) {
 
 int swiglu_last_cuda_error(void) { return g_last_cuda_error; }
 
-int swiglu_abi_version(void) { return 1; }
+int swiglu_abi_version(void) { return 2; }
 
 }  // extern "C"

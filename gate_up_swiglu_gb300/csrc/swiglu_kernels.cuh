@@ -283,25 +283,34 @@ __device__ __forceinline__ void store_pack(uint32_t *w, const float *v) {
 // and advances by gridDim * U * kThreads packs per iteration; (row, column)
 // of each of its U packs is carried along incrementally (step_q rows plus
 // step_r packs, with one carry), so the loop needs no division.
+// The gate and up operands are addressed separately (base pointer and row
+// stride each), which covers both the fused [rows, 2n] buffer (up = gate + n,
+// same stride) and two separate tensors.
 struct FwdParams {
-    const void *x;
+    const void *g;
+    const void *u;
     void *y;
     int64_t rows;
-    int64_t x_stride;  // row strides, in packs
+    int64_t g_stride;  // row strides, in packs
+    int64_t u_stride;
     int64_t y_stride;
     int64_t step_q;    // (gridDim * U * kThreads) / nvec
-    int32_t nvec;      // packs per half-row (n / VEC)
+    int32_t nvec;      // packs per row of each operand (n / VEC)
     int32_t step_r;    // (gridDim * U * kThreads) % nvec
 };
 
 struct BwdParams {
     const void *dy;
-    const void *x;
-    void *dx;  // == x for the in-place backward
+    const void *g;
+    const void *u;
+    void *dg;  // == g for the in-place backward
+    void *du;  // == u for the in-place backward
     int64_t rows;
     int64_t dy_stride;  // row strides, in packs
-    int64_t x_stride;
-    int64_t dx_stride;
+    int64_t g_stride;
+    int64_t u_stride;
+    int64_t dg_stride;
+    int64_t du_stride;
     int64_t step_q;
     int32_t nvec;
     int32_t step_r;
@@ -338,9 +347,9 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
     constexpr int NW = (B + 3) / 4;
     using L = Ld<B, LD>;
     using S = St<B, ST>;
-    const char *x = static_cast<const char *>(p.x);
+    const char *gp = static_cast<const char *>(p.g);
+    const char *up = static_cast<const char *>(p.u);
     char *y = static_cast<char *>(p.y);
-    const int64_t up_off = (int64_t)p.nvec * B;
 
     int64_t r[U];
     int32_t c[U];
@@ -350,9 +359,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
-                const char *px = x + (r[k] * p.x_stride + c[k]) * B;
-                L::run(px, g[k]);
-                L::run(px + up_off, u[k]);
+                L::run(gp + (r[k] * p.g_stride + c[k]) * B, g[k]);
+                L::run(up + (r[k] * p.u_stride + c[k]) * B, u[k]);
             }
         }
 #pragma unroll
@@ -373,9 +381,9 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
     }
 }
 
-// IN_PLACE selects nothing but the aliasing contract (dx == x, so LD must be
-// a coherent kind); the arithmetic is the same template body, so both
-// instances give identical bits.
+// IN_PLACE selects nothing but the aliasing contract (an output may be the
+// very buffer of the matching input, so LD must be a coherent kind); the
+// arithmetic is the same template body, so both instances give identical bits.
 template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
 __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p) {
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256),
@@ -385,9 +393,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
     using L = Ld<B, LD>;
     using S = St<B, ST>;
     const char *dy = static_cast<const char *>(p.dy);
-    const char *x = static_cast<const char *>(p.x);
-    char *dx = IN_PLACE ? const_cast<char *>(x) : static_cast<char *>(p.dx);
-    const int64_t up_off = (int64_t)p.nvec * B;
+    const char *gp = static_cast<const char *>(p.g);
+    const char *up = static_cast<const char *>(p.u);
+    char *dg = static_cast<char *>(p.dg);
+    char *du = static_cast<char *>(p.du);
 
     int64_t r[U];
     int32_t c[U];
@@ -397,10 +406,9 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
-                const char *px = x + (r[k] * p.x_stride + c[k]) * B;
                 L::run(dy + (r[k] * p.dy_stride + c[k]) * B, d[k]);
-                L::run(px, g[k]);
-                L::run(px + up_off, u[k]);
+                L::run(gp + (r[k] * p.g_stride + c[k]) * B, g[k]);
+                L::run(up + (r[k] * p.u_stride + c[k]) * B, u[k]);
             }
         }
 #pragma unroll
@@ -419,9 +427,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
                 }
                 store_pack<E, VEC>(og, gv);
                 store_pack<E, VEC>(ou, uv);
-                char *pdx = dx + (r[k] * p.dx_stride + c[k]) * B;
-                S::run(pdx, og);
-                S::run(pdx + up_off, ou);
+                S::run(dg + (r[k] * p.dg_stride + c[k]) * B, og);
+                S::run(du + (r[k] * p.du_stride + c[k]) * B, ou);
             }
         }
         advance<U>(p.step_q, p.step_r, p.nvec, r, c);

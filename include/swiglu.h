@@ -97,6 +97,33 @@ swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64
                                   int64_t dx_row_stride, swiglu_dtype_t dtype, int in_place,
                                   swiglu_stream_t stream);
 
+/*
+ * Two-tensor form (Liger-Kernel Megatron SwiGLU page, §Background: the gate
+ * and the up projection arrive as two separate tensors a and b, as HuggingFace
+ * models produce them).  Same arithmetic as the fused form:
+ *   c[r, j]  = silu(a[r, j]) * b[r, j]
+ *   da[r, j] = dc * b * s * (1 + a * (1 - s)),  db[r, j] = dc * a * s
+ * for r < rows, j < n; every tensor is [rows, n] with its own row stride
+ * (>= n, elements).  a and b may overlap each other (they are only read).
+ *   forward:  c must not overlap a or b (SWIGLU_ERR_ALIAS).
+ *   backward: da may be exactly a (same pointer and stride) and db exactly b,
+ *             giving the in-place form (bit-identical to the out-of-place one);
+ *             apart from that an output may overlap no input and not the other
+ *             output (SWIGLU_ERR_ALIAS).
+ * For the fused [rows, 2n] layout use swiglu_gateup_*: its halves interleave
+ * row by row, which these byte-range overlap rules would reject.
+ */
+swiglu_status_t swiglu_silu_mul_fwd(const void *a, const void *b, void *c, int64_t rows, int64_t n,
+                                    int64_t a_row_stride, int64_t b_row_stride,
+                                    int64_t c_row_stride, swiglu_dtype_t dtype,
+                                    swiglu_stream_t stream);
+
+swiglu_status_t swiglu_silu_mul_bwd(const void *dc, const void *a, const void *b, void *da,
+                                    void *db, int64_t rows, int64_t n, int64_t dc_row_stride,
+                                    int64_t a_row_stride, int64_t b_row_stride,
+                                    int64_t da_row_stride, int64_t db_row_stride,
+                                    swiglu_dtype_t dtype, swiglu_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 const char *swiglu_status_string(swiglu_status_t status);
 

@@ -32,8 +32,8 @@ def declared_functions():
 
 def test_header_declares_expected_calls():
     assert declared_functions() == sorted(
-        ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_status_string",
-         "swiglu_last_cuda_error", "swiglu_abi_version"])
+        ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
+         "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
 
 
 def test_library_exports_every_declared_symbol(sw):
@@ -53,7 +53,7 @@ def test_status_strings(sw):
         s = sw.status_string(code)
         assert s and s != "unknown status"
     assert sw.status_string(-99) == "unknown status"
-    assert sw.lib.swiglu_abi_version() == 1
+    assert sw.lib.swiglu_abi_version() == 2
     assert sw.lib.swiglu_last_cuda_error() == 0
 
 
@@ -111,6 +111,38 @@ def test_bwd_rejections(sw):
     assert bwd(sw, ip=1, dx=DX) == -5
     assert bwd(sw, ip=1, dx=X, sdx=24) == -4
     assert bwd(sw, ip=1, dx=X, dy=X + 16) == -5
+
+
+A, B, C, DA, DB = X, Y, DY, DX, 0x50_0000_0000
+
+
+def mfwd(sw, a=A, b=B, c=C, rows=4, n=8, sa=8, sb=8, sc=8, dt=BF16):
+    return sw.lib.swiglu_silu_mul_fwd(a, b, c, rows, n, sa, sb, sc, dt, None)
+
+
+def mbwd(sw, dc=DY, a=A, b=B, da=DA, db=DB, rows=4, n=8, s=(8, 8, 8, 8, 8), dt=BF16):
+    return sw.lib.swiglu_silu_mul_bwd(dc, a, b, da, db, rows, n, *s, dt, None)
+
+
+def test_two_tensor_rejections(sw):
+    assert mfwd(sw, a=None, rows=0) == 0
+    assert mfwd(sw, dt=5) == -2
+    assert mfwd(sw, n=-2) == -3
+    assert mfwd(sw, b=None) == -1
+    assert mfwd(sw, sb=7) == -4
+    assert mfwd(sw, c=A + 16) == -5
+    assert mfwd(sw, c=B) == -5
+    assert mbwd(sw, rows=0, da=None) == 0
+    assert mbwd(sw, db=None) == -1
+    assert mbwd(sw, s=(8, 8, 8, 7, 8)) == -4
+    # outputs: no overlap with each other, with dc, or with the other input
+    assert mbwd(sw, db=DA + 8) == -5
+    assert mbwd(sw, da=DY) == -5
+    assert mbwd(sw, da=B) == -5
+    assert mbwd(sw, db=A + 2) == -5
+    # da partially over a is rejected; exactly a (same stride) is the in-place form
+    assert mbwd(sw, da=A + 2) == -5
+    assert mbwd(sw, da=A, s=(8, 8, 8, 16, 8)) == -5
 
 
 def test_import_fails_loudly_without_the_library(tmp_path):
