@@ -326,6 +326,8 @@ def ours_arm(args, w):
     del x_saved
     ip_avg = max_over_ranks(statistics.mean(ip_ms))
 
+    extras = measure_extras(sw, w, x, dy, dev, stream, reps=min(K, 100))
+
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(sw, w, x, dy, dev, K=min(K, 20), barrier=barrier, reduce=max_over_ranks)
@@ -367,6 +369,7 @@ def ours_arm(args, w):
                      "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(bwd_gbs / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes": bb},
+        "extras": extras,
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
@@ -375,6 +378,58 @@ def ours_arm(args, w):
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def _event_ms(fn, stream, reps):
+    """Mean CUDA-event time of fn() on `stream` over `reps` launches (after 3
+    warm-up calls)."""
+    for _ in range(3):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_extras(sw, w, x, dy, dev, stream, reps):
+    """The other rows on the same workload: the two-tensor entry points on
+    separate gate / up tensors (HuggingFace layout), and one forward + backward
+    through the autograd module (wrapper overhead over the raw C ABI)."""
+    peak, _ = measured_peaks()
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    n = w.n
+    a = x[:, :n].contiguous()
+    b = x[:, n:].contiguous()
+    c = torch.empty_like(a)
+    da, db = torch.empty_like(a), torch.empty_like(b)
+    f_ms = _event_ms(lambda: sw.swiglu_silu_mul_fwd(a, b, c, stream=stream), stream, reps)
+    b_ms = _event_ms(lambda: sw.swiglu_silu_mul_bwd(dy, a, b, da, db, stream=stream), stream, reps)
+    del a, b, c, da, db
+    from gate_up_swiglu_gb300.autograd import GateUpSwiGLU
+
+    mod = GateUpSwiGLU()
+    xs = x.view(*w.shape).detach().requires_grad_(True)
+    dys = dy.view(*w.shape[:-1], n)
+
+    def ag_step():
+        y = mod(xs)
+        torch.autograd.grad(y, xs, dys)
+
+    ag_ms = _event_ms(ag_step, stream, reps)
+    return {
+        "silu_mul_separate_tensors": {
+            "layout": "gate and up as two contiguous [rows, n] tensors", "reps": reps,
+            "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
+            "fwd_gbs": round(gbs(w.fwd_bytes(), f_ms), 1), "bwd_gbs": round(gbs(w.bwd_bytes(), b_ms), 1),
+            "fwd_frac_of_measured": round(gbs(w.fwd_bytes(), f_ms) / peak, 4),
+            "bwd_frac_of_measured": round(gbs(w.bwd_bytes(), b_ms) / peak, 4)},
+        "autograd_module_fwd_bwd": {
+            "what": "GateUpSwiGLU forward + torch.autograd.grad, 3D input, out of place",
+            "reps": reps, "ms": round(ag_ms, 4)},
+    }
 
 
 def l2_note(w: W.Workload) -> str:

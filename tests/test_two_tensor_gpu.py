@@ -99,6 +99,8 @@ def test_two_tensor_errors(sw):
     with pytest.raises(sw.SwigluError) as e:
         sw.swiglu_silu_mul_fwd(a, a, a)
     assert e.value.status == -5
-    with pytest.raises(sw.SwigluError) as e:
-        sw.swiglu_silu_mul_bwd(a.clone(), a, a.clone(), da=a[:, 1:].contiguous(), db=a)
+    base = torch.randn(4, 9, device="cuda")
+    a2 = base[:, :8]
+    with pytest.raises(sw.SwigluError) as e:  # da shifted one element over a
+        sw.swiglu_silu_mul_bwd(a.clone(), a2, a.clone(), da=base[:, 1:9])
     assert e.value.status == -5
