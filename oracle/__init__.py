@@ -67,6 +67,16 @@ def load(path: str = None):
         lib.oracle_silu_mul_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64,
                                             ctypes.c_int]
         lib.oracle_silu_mul_bwd.restype = ctypes.c_int
+        lib.oracle_swiglu_weighted_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_swiglu_weighted_fwd.restype = ctypes.c_int
+        lib.oracle_swiglu_weighted_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                   ctypes.c_int]
+        lib.oracle_swiglu_weighted_bwd.restype = ctypes.c_int
+        lib.oracle_swiglu_bias_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_int]
+        lib.oracle_swiglu_bias_fwd.restype = ctypes.c_int
+        lib.oracle_swiglu_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                               ctypes.c_int]
+        lib.oracle_swiglu_bias_bwd.restype = ctypes.c_int
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         if path is None:
@@ -144,6 +154,81 @@ def silu_mul_bwd(dc, a, b, da=None, db=None, lib=None):
     if rc != 0:
         raise ValueError("oracle_silu_mul_bwd rejected its arguments")
     return da, db
+
+
+def _vec(t: torch.Tensor, name: str, dtype, size: int) -> None:
+    if t.device.type != "cpu" or t.dtype != dtype or t.dim() != 1 or t.numel() != size or \
+            (size > 1 and t.stride(0) != 1):
+        raise ValueError(f"oracle: {name} must be a contiguous CPU {dtype} vector of {size}")
+
+
+def weighted_fwd(x: torch.Tensor, w: torch.Tensor, lib=None) -> torch.Tensor:
+    """y[r, j] = w[r] * silu(x[r, j]) * x[r, n + j]; w fp32 [rows]."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(w, "w", torch.float32, rows)
+    y = torch.empty((rows, n), dtype=x.dtype)
+    rc = lib.oracle_swiglu_weighted_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, n,
+                                        x.stride(0), y.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_weighted_fwd rejected its arguments")
+    return y
+
+
+def weighted_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor = None,
+                 lib=None):
+    """Returns (dx, dw): dx of the weighted activation, dw fp32 [rows]."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    _rowmajor(dy, "dy")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(w, "w", torch.float32, rows)
+    dx = torch.empty((rows, 2 * n), dtype=x.dtype) if dx is None else dx
+    dw = torch.empty(rows, dtype=torch.float32)
+    rc = lib.oracle_swiglu_weighted_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
+                                        dw.data_ptr(), rows, n, dy.stride(0), x.stride(0),
+                                        dx.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_weighted_bwd rejected its arguments")
+    return dx, dw
+
+
+def bias_fwd(x: torch.Tensor, bias: torch.Tensor, lib=None) -> torch.Tensor:
+    """y = silu(g + bias[:n]) * (u + bias[n:]); bias [2n] in x's dtype."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(bias, "bias", x.dtype, 2 * n)
+    y = torch.empty((rows, n), dtype=x.dtype)
+    rc = lib.oracle_swiglu_bias_fwd(x.data_ptr(), bias.data_ptr(), y.data_ptr(), rows, n,
+                                    x.stride(0), y.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_bias_fwd rejected its arguments")
+    return y
+
+
+def bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor, dx: torch.Tensor = None,
+             lib=None):
+    """Returns (dx, dbias): dbias[k] = sum over rows of the exact dx[:, k]."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    _rowmajor(dy, "dy")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(bias, "bias", x.dtype, 2 * n)
+    dx = torch.empty((rows, 2 * n), dtype=x.dtype) if dx is None else dx
+    dbias = torch.empty(2 * n, dtype=x.dtype)
+    acc = torch.empty(2 * n, dtype=torch.float64)
+    rc = lib.oracle_swiglu_bias_bwd(dy.data_ptr(), x.data_ptr(), bias.data_ptr(), dx.data_ptr(),
+                                    dbias.data_ptr(), acc.data_ptr(), rows, n, dy.stride(0),
+                                    x.stride(0), dx.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_bias_bwd rejected its arguments")
+    return dx, dbias
 
 
 def bf16_from_double(v: float, lib=None) -> int:

@@ -199,3 +199,94 @@ int oracle_silu_mul_bwd(const void *dc, const void *a, const void *b, void *da, 
     }
     return ORACLE_OK;
 }
+
+/* ---- per-token weights and bias ------------------------------------------ */
+/* Liger-Kernel Megatron SwiGLU page, §Known issues 2: Megatron's MoE routed
+ * experts scale each token's activation by its routing weight
+ * (weighted_bias_swiglu_impl needs a per_token_scale-aware kernel); §Scope:
+ * the fused path has no bias and falls back when one is given.  Both are
+ * stated here by their plain definitions:
+ *
+ *   weighted:  y[r, j] = w[r] * silu(g) * u
+ *              d gate = dy * w[r] * u * s * (1 + g (1 - s)),  d up = dy * w[r] * g * s
+ *              dw[r]  = sum_j dy[r, j] * silu(g[r, j]) * u[r, j]
+ *   bias:      z_g = g + bias[j], z_u = u + bias[n + j];  y = silu(z_g) * z_u
+ *              dx = the plain backward evaluated at (z_g, z_u)
+ *              dbias[k] = sum_r dx[r, k]   (k < 2n, the exact dx before rounding)
+ *
+ * w and dw are fp32 [rows] (unit stride); bias and dbias have x's dtype, [2n].
+ * Sums are accumulated in double and rounded once. */
+
+int oracle_swiglu_weighted_fwd(const void *x, const float *w, void *y, int64_t rows, int64_t n,
+                               int64_t sx, int64_t sy, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double wr = (double)w[r];
+        for (int64_t j = 0; j < n; ++j) {
+            double g = load_elem(x, r * sx + j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype);
+            store_elem(y, r * sy + j, dtype, wr * swiglu_fwd_pair(g, u));
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_swiglu_weighted_bwd(const void *dy, const void *x, const float *w, void *dx, float *dw,
+                               int64_t rows, int64_t n, int64_t sdy, int64_t sx, int64_t sdx,
+                               int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double wr = (double)w[r];
+        double acc = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            double d = load_elem(dy, r * sdy + j, dtype);
+            double g = load_elem(x, r * sx + j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype);
+            double dg, du;
+            acc += d * swiglu_fwd_pair(g, u);
+            swiglu_bwd_pair(d * wr, g, u, &dg, &du);
+            store_elem(dx, r * sdx + j, dtype, dg);
+            store_elem(dx, r * sdx + n + j, dtype, du);
+        }
+        dw[r] = (float)acc;
+    }
+    return ORACLE_OK;
+}
+
+int oracle_swiglu_bias_fwd(const void *x, const void *bias, void *y, int64_t rows, int64_t n,
+                           int64_t sx, int64_t sy, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double g = load_elem(x, r * sx + j, dtype) + load_elem(bias, j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);
+            store_elem(y, r * sy + j, dtype, swiglu_fwd_pair(g, u));
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* dbias needs the unrounded dx of every row; `acc` is caller-provided
+ * scratch of 2n doubles (the oracle keeps its own arithmetic simple rather
+ * than allocate). */
+int oracle_swiglu_bias_bwd(const void *dy, const void *x, const void *bias, void *dx, void *dbias,
+                           double *acc, int64_t rows, int64_t n, int64_t sdy, int64_t sx,
+                           int64_t sdx, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t k = 0; k < 2 * n; ++k) acc[k] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < n; ++j) {
+            double d = load_elem(dy, r * sdy + j, dtype);
+            double g = load_elem(x, r * sx + j, dtype) + load_elem(bias, j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);
+            double dg, du;
+            swiglu_bwd_pair(d, g, u, &dg, &du);
+            acc[j] += dg;
+            acc[n + j] += du;
+            store_elem(dx, r * sdx + j, dtype, dg);
+            store_elem(dx, r * sdx + n + j, dtype, du);
+        }
+    }
+    for (int64_t k = 0; k < 2 * n; ++k) store_elem(dbias, k, dtype, acc[k]);
+    return ORACLE_OK;
+}

@@ -305,9 +305,60 @@ def pin_two_tensor_form(lib):
         assert torch.equal(ai, da2) and torch.equal(bi, db2)
 
 
+def pin_weighted(lib):
+    """Per-token weights: torch float64 autograd of w[:, None] * F.silu(a) * b
+    gives y, the input gradient and dw; w = 1 reduces to the plain form."""
+    for seed, (rows, n) in enumerate([(11, 37), (3, 1), (2, 500)]):
+        x = _rand((rows, 2 * n), 100 + seed, 3.0)
+        dy = _rand((rows, n), 110 + seed)
+        w = _rand((rows,), 120 + seed).float()
+        a, b = [t.clone().requires_grad_(True) for t in x.chunk(2, dim=-1)]
+        wt = w.double().clone().requires_grad_(True)
+        ref = wt[:, None] * F.silu(a) * b
+        ref.backward(dy)
+        y = oracle.weighted_fwd(x, w, lib=lib)
+        dx, dw = oracle.weighted_bwd(dy, x, w, lib=lib)
+        assert torch.allclose(y, ref.detach(), rtol=1e-13, atol=1e-300)
+        assert torch.allclose(dx[:, :n], a.grad, rtol=1e-12, atol=1e-14)
+        assert torch.allclose(dx[:, n:], b.grad, rtol=1e-12, atol=1e-300)
+        assert torch.allclose(dw.double(), wt.grad, rtol=2e-7, atol=1e-30)
+        one = torch.ones(rows)
+        assert torch.equal(oracle.weighted_fwd(x, one, lib=lib), oracle.fwd(x, lib=lib))
+        assert torch.equal(oracle.weighted_bwd(dy, x, one, lib=lib)[0], oracle.bwd(dy, x, lib=lib))
+
+
+def pin_bias(lib):
+    """Bias: torch float64 autograd of F.silu(a + bias[:n]) * (b + bias[n:])
+    gives y, dx and the bias gradient (summed over rows); zero bias reduces to
+    the plain form."""
+    for seed, (rows, n) in enumerate([(13, 21), (1, 3), (40, 7)]):
+        x = _rand((rows, 2 * n), 130 + seed, 3.0)
+        dy = _rand((rows, n), 140 + seed)
+        bias = _rand((2 * n,), 150 + seed)
+        a, b = [t.clone().requires_grad_(True) for t in x.chunk(2, dim=-1)]
+        bt = bias.clone().requires_grad_(True)
+        ref = F.silu(a + bt[:n]) * (b + bt[n:])
+        ref.backward(dy)
+        y = oracle.bias_fwd(x, bias, lib=lib)
+        dx, db = oracle.bias_bwd(dy, x, bias, lib=lib)
+        assert torch.allclose(y, ref.detach(), rtol=1e-12, atol=1e-300)
+        assert torch.allclose(dx[:, :n], a.grad, rtol=1e-11, atol=1e-13)
+        assert torch.allclose(dx[:, n:], b.grad, rtol=1e-12, atol=1e-300)
+        assert torch.allclose(db, bt.grad, rtol=1e-11, atol=1e-13)
+        zero = torch.zeros(2 * n, dtype=F64)
+        assert torch.equal(oracle.bias_fwd(x, zero, lib=lib), oracle.fwd(x, lib=lib))
+        assert torch.equal(oracle.bias_bwd(dy, x, zero, lib=lib)[0], oracle.bwd(dy, x, lib=lib))
+        # bf16: dbias is the once-rounded sum of the unrounded gradients
+        xb, dyb, bb = x.to(torch.bfloat16), dy.to(torch.bfloat16), bias.to(torch.bfloat16)
+        dx64, db64 = oracle.bias_bwd(dyb.double(), xb.double(), bb.double(), lib=lib)
+        dxb, dbb = oracle.bias_bwd(dyb, xb, bb, lib=lib)
+        assert torch.equal(_bf16_bits(dbb),
+                           torch.tensor([oracle.bf16_from_double(float(v), lib=lib) for v in db64]))
+
+
 PINS = [pin_zero_gate, pin_saturation, pin_stationary_point, pin_finite_differences,
         pin_torch_two_tensor, pin_bf16_rounding_brute, pin_rounding_matches_torch,
-        pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form]
+        pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form, pin_weighted, pin_bias]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -343,6 +394,11 @@ MUTATIONS = {
     "two_tensor_a_b_swapped": ("double g = load_elem(a, r * sa + j, dtype);\n            double u = load_elem(b, r * sb + j, dtype);\n            store_elem(c",
                                "double g = load_elem(b, r * sb + j, dtype);\n            double u = load_elem(a, r * sa + j, dtype);\n            store_elem(c"),
     "two_tensor_db_stride": ("store_elem(db, r * sdb + j", "store_elem(db, r * sda + j"),
+    "weighted_dw_without_u": ("acc += d * swiglu_fwd_pair(g, u);", "acc += d * swiglu_fwd_pair(g, 1.0);"),
+    "weighted_grad_unscaled": ("swiglu_bwd_pair(d * wr, g, u, &dg, &du);", "swiglu_bwd_pair(d, g, u, &dg, &du);"),
+    "bias_halves_swapped": ("double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);\n            store_elem(y",
+                            "double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, j, dtype);\n            store_elem(y"),
+    "dbias_last_row_only": ("            acc[j] += dg;\n            acc[n + j] += du;", "            acc[j] = dg;\n            acc[n + j] = du;"),
 }
 
 
