@@ -146,18 +146,46 @@ struct Operand {
 struct FwdArgs {
     Operand g, u, y;
     int64_t rows, n;
+    int mode = swiglu::kPlain;
+    const void *bias_g = nullptr, *bias_u = nullptr;  // kBias
+    const float *w = nullptr;                          // kWeight
 };
 
 struct BwdArgs {
     Operand dy, g, u, dg, du;
     int64_t rows, n;
+    int mode = swiglu::kPlain;
+    const void *bias_g = nullptr, *bias_u = nullptr;  // kBias
+    void *dbias = nullptr;
+    float *partial = nullptr;                          // kBias workspace
+    const float *w = nullptr;                          // kWeight
+    float *dw = nullptr;
 };
 
-template <typename E, int VEC>
+// Row groups of the bias backward: enough (column tile, row group) CTAs to
+// fill every SM with kBwdPolicy.max_ctas_per_sm of them, once.
+struct BiasPlan {
+    int64_t tiles, groups, rows_per_group;
+    size_t workspace_bytes;
+};
+
+BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {
+    BiasPlan b;
+    b.tiles = (n + swiglu::kBiasTileCols - 1) / swiglu::kBiasTileCols;
+    int64_t groups = ((int64_t)sms * kBwdPolicy.max_ctas_per_sm) / b.tiles;
+    if (groups < 1) groups = 1;
+    if (groups > rows) groups = rows;
+    b.rows_per_group = (rows + groups - 1) / groups;
+    b.groups = (rows + b.rows_per_group - 1) / b.rows_per_group;
+    b.workspace_bytes = (size_t)b.groups * (size_t)(2 * n) * sizeof(float);
+    return b;
+}
+
+template <typename E, int VEC, int MODE>
 swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
-    auto kernel = swiglu::swiglu_fwd_kernel<E, VEC, U, kLoadOutOfPlace, kStore>;
+    auto kernel = swiglu::swiglu_fwd_kernel<E, VEC, U, kLoadOutOfPlace, kStore, MODE>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -172,6 +200,9 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     p.g = a.g.p;
     p.u = a.u.p;
     p.y = const_cast<void *>(a.y.p);
+    p.bias_g = a.bias_g;
+    p.bias_u = a.bias_u;
+    p.w = a.w;
     p.rows = a.rows;
     p.g_stride = a.g.stride / VEC;
     p.u_stride = a.u.stride / VEC;
@@ -184,8 +215,32 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
+swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
+    swiglu::BwdParams p;
+    p.dy = a.dy.p;
+    p.g = a.g.p;
+    p.u = a.u.p;
+    p.dg = const_cast<void *>(a.dg.p);
+    p.du = const_cast<void *>(a.du.p);
+    p.bias_g = a.bias_g;
+    p.bias_u = a.bias_u;
+    p.w = a.w;
+    p.dw = a.dw;
+    p.partial = a.partial;
+    p.rows = a.rows;
+    p.dy_stride = a.dy.stride / vec;
+    p.g_stride = a.g.stride / vec;
+    p.u_stride = a.u.stride / vec;
+    p.dg_stride = a.dg.stride / vec;
+    p.du_stride = a.du.stride / vec;
+    p.nvec = (int32_t)(a.n / vec);
+    p.step_q = 0;
+    p.step_r = 0;
+    return p;
+}
+
 template <typename E, int VEC, bool IN_PLACE>
-swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
+swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
     auto kernel = swiglu::swiglu_bwd_kernel<E, VEC, U, IN_PLACE,
@@ -200,46 +255,92 @@ swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
-    swiglu::BwdParams p;
-    p.dy = a.dy.p;
-    p.g = a.g.p;
-    p.u = a.u.p;
-    p.dg = const_cast<void *>(a.dg.p);
-    p.du = const_cast<void *>(a.du.p);
-    p.rows = a.rows;
-    p.dy_stride = a.dy.stride / VEC;
-    p.g_stride = a.g.stride / VEC;
-    p.u_stride = a.u.stride / VEC;
-    p.dg_stride = a.dg.stride / VEC;
-    p.du_stride = a.du.stride / VEC;
+    swiglu::BwdParams p = bwd_params(a, VEC);
     p.step_q = step / nvec;
-    p.nvec = (int32_t)nvec;
     p.step_r = (int32_t)(step % nvec);
     kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
-// The widest pack every operand allows (pick_vec never returns more than
-// max_pack_bytes / kBytes elements, so only those widths are instantiated).
+template <typename E, int VEC, bool IN_PLACE>
+swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
+    constexpr int U = unroll_for(E::kBytes * VEC);
+    static std::atomic<int> occ[kMaxDevices];
+    auto kernel = swiglu::swiglu_bwd_weighted_kernel<E, VEC, U, IN_PLACE,
+                                                     IN_PLACE ? kLoadInPlace : kLoadOutOfPlace,
+                                                     kStore>;
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int per_sm = 0;
+    e = ctas_per_sm(kernel, d, occ, per_sm);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm > kBwdPolicy.max_ctas_per_sm) per_sm = kBwdPolicy.max_ctas_per_sm;
+    int64_t grid = (int64_t)d.sms * per_sm;
+    if (grid > a.rows) grid = a.rows;
+    kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(bwd_params(a, VEC));
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+}
+
+template <typename E, int VEC, bool IN_PLACE>
+swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
+    auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
+                                                 IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore>;
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const BiasPlan b = bias_plan(a.rows, a.n, d.sms);
+    kernel<<<(unsigned)(b.tiles * b.groups), swiglu::kThreads, 0, stream>>>(
+        bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    int64_t rgrid = (2 * a.n + swiglu::kThreads - 1) / swiglu::kThreads;
+    if (rgrid > (int64_t)d.sms * 8) rgrid = (int64_t)d.sms * 8;
+    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)rgrid, swiglu::kThreads, 0, stream>>>(
+        a.partial, b.groups, 2 * a.n, a.dbias);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+}
+
+template <typename E, int VEC, bool IN_PLACE>
+swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
+    if (a.mode == swiglu::kWeight) return launch_bwd_weighted<E, VEC, IN_PLACE>(a, stream);
+    if (a.mode == swiglu::kBias) return launch_bwd_bias<E, VEC, IN_PLACE>(a, stream);
+    return launch_bwd_plain<E, VEC, IN_PLACE>(a, stream);
+}
+
+template <typename E, int VEC>
+swiglu_status_t launch_fwd_mode(const FwdArgs &a, cudaStream_t st) {
+    if (a.mode == swiglu::kWeight) return launch_fwd<E, VEC, swiglu::kWeight>(a, st);
+    if (a.mode == swiglu::kBias) return launch_fwd<E, VEC, swiglu::kBias>(a, st);
+    return launch_fwd<E, VEC, swiglu::kPlain>(a, st);
+}
+
+// The widest pack every operand (bias halves included) allows; pick_vec never
+// returns more than max_pack_bytes / kBytes elements, so only those widths are
+// instantiated.
 template <typename E>
 swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const int64_t strides[3] = {a.g.stride, a.u.stride, a.y.stride};
-    const void *ptrs[3] = {a.g.p, a.u.p, a.y.p};
-    const int vec = pick_vec(E::kBytes, kFwdPolicy.max_pack_bytes, a.n, strides, 3, ptrs, 3);
+    const void *ptrs[5] = {a.g.p, a.u.p, a.y.p, a.bias_g, a.bias_u};
+    const int np = a.mode == swiglu::kBias ? 5 : 3;
+    const int vec = pick_vec(E::kBytes, kFwdPolicy.max_pack_bytes, a.n, strides, 3, ptrs, np);
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
-    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd<E, 16>(a, st);
-    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd<E, 8>(a, st);
-    if (vec == 4) return launch_fwd<E, 4>(a, st);
-    if (vec == 2) return launch_fwd<E, 2>(a, st);
-    return launch_fwd<E, 1>(a, st);
+    if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);
+    if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd_mode<E, 8>(a, st);
+    if (vec == 4) return launch_fwd_mode<E, 4>(a, st);
+    if (vec == 2) return launch_fwd_mode<E, 2>(a, st);
+    return launch_fwd_mode<E, 1>(a, st);
 }
 
 template <typename E, bool IP>
 swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     const int64_t strides[5] = {a.dy.stride, a.g.stride, a.u.stride, a.dg.stride, a.du.stride};
-    const void *ptrs[5] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p};
-    const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, 5);
+    const void *ptrs[7] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p, a.bias_g, a.bias_u};
+    const int np = a.mode == swiglu::kBias ? 7 : 5;
+    const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, np);
     constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_bwd<E, 16, IP>(a, st);
     if constexpr (kMaxVec >= 8) if (vec == 8) return launch_bwd<E, 8, IP>(a, st);
@@ -266,6 +367,42 @@ swiglu_status_t run_bwd(swiglu_dtype_t dtype, bool in_place, const BwdArgs &a,
 swiglu_status_t check_common(swiglu_dtype_t dtype, int64_t rows, int64_t n) {
     if (elem_bytes(dtype) == 0) return SWIGLU_ERR_DTYPE;
     if (rows < 0 || n < 0 || n > SWIGLU_MAX_N) return SWIGLU_ERR_SHAPE;
+    return SWIGLU_OK;
+}
+
+// Validates the fused backward's dy / x / dx (with the in-place contract) and
+// fills `a` with the fused layout's operands; sp[] = spans of dy, x, dx.
+swiglu_status_t gateup_bwd_args(const void *dy, const void *x, void *dx, int64_t rows, int64_t n,
+                                int64_t dy_row_stride, int64_t x_row_stride,
+                                int64_t dx_row_stride, swiglu_dtype_t dtype, int in_place,
+                                BwdArgs &a, Span sp[3]) {
+    const int eb = elem_bytes(dtype);
+    if (in_place) {
+        if (dx == nullptr) dx = const_cast<void *>(x);
+        if (dx_row_stride == 0) dx_row_stride = x_row_stride;
+    }
+    if (dy == nullptr || x == nullptr || dx == nullptr) return SWIGLU_ERR_NULL;
+    if (dy_row_stride < n || x_row_stride < 2 * n || dx_row_stride < 2 * n) return SWIGLU_ERR_STRIDE;
+    if (!span_of(dy, rows, n, dy_row_stride, eb, sp[0]) ||
+        !span_of(x, rows, 2 * n, x_row_stride, eb, sp[1]) ||
+        !span_of(dx, rows, 2 * n, dx_row_stride, eb, sp[2]))
+        return SWIGLU_ERR_SHAPE;
+    if (in_place) {
+        if (dx != x) return SWIGLU_ERR_ALIAS;
+        if (dx_row_stride != x_row_stride) return SWIGLU_ERR_STRIDE;
+        if (overlaps(sp[0], sp[1])) return SWIGLU_ERR_ALIAS;
+    } else {
+        if (overlaps(sp[2], sp[1]) || overlaps(sp[2], sp[0])) return SWIGLU_ERR_ALIAS;
+    }
+    const char *xb = static_cast<const char *>(x);
+    char *dxb = static_cast<char *>(dx);
+    a.dy = {dy, dy_row_stride};
+    a.g = {x, x_row_stride};
+    a.u = {xb + n * eb, x_row_stride};
+    a.dg = {dx, dx_row_stride};
+    a.du = {dxb + n * eb, dx_row_stride};
+    a.rows = rows;
+    a.n = n;
     return SWIGLU_OK;
 }
 
@@ -298,34 +435,146 @@ swiglu_status_t swiglu_gateup_bwd(const void *dy, const void *x, void *dx, int64
     swiglu_status_t st = check_common(dtype, rows, n);
     if (st != SWIGLU_OK) return st;
     if (rows == 0 || n == 0) return SWIGLU_OK;
+    BwdArgs a;
+    Span sp[3];
+    st = gateup_bwd_args(dy, x, dx, rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
+                         in_place, a, sp);
+    if (st != SWIGLU_OK) return st;
+    return run_bwd(dtype, in_place != 0, a, stream);
+}
+
+swiglu_status_t swiglu_gateup_weighted_fwd(const void *x, const float *w, void *y, int64_t rows,
+                                           int64_t n, int64_t x_row_stride, int64_t y_row_stride,
+                                           swiglu_dtype_t dtype, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
     const int eb = elem_bytes(dtype);
-    if (in_place) {
-        if (dx == nullptr) dx = const_cast<void *>(x);
-        if (dx_row_stride == 0) dx_row_stride = x_row_stride;
-    }
-    if (dy == nullptr || x == nullptr || dx == nullptr) return SWIGLU_ERR_NULL;
-    if (dy_row_stride < n || x_row_stride < 2 * n || dx_row_stride < 2 * n) return SWIGLU_ERR_STRIDE;
-    Span sdys, sxs, sdxs;
-    if (!span_of(dy, rows, n, dy_row_stride, eb, sdys) ||
-        !span_of(x, rows, 2 * n, x_row_stride, eb, sxs) ||
-        !span_of(dx, rows, 2 * n, dx_row_stride, eb, sdxs))
+    if (x == nullptr || y == nullptr || w == nullptr) return SWIGLU_ERR_NULL;
+    if (x_row_stride < 2 * n || y_row_stride < n) return SWIGLU_ERR_STRIDE;
+    Span sxs, sys, sws;
+    if (!span_of(x, rows, 2 * n, x_row_stride, eb, sxs) ||
+        !span_of(y, rows, n, y_row_stride, eb, sys) || !span_of(w, 1, rows, rows, 4, sws))
         return SWIGLU_ERR_SHAPE;
-    if (in_place) {
-        if (dx != x) return SWIGLU_ERR_ALIAS;
-        if (dx_row_stride != x_row_stride) return SWIGLU_ERR_STRIDE;
-        if (overlaps(sdys, sxs)) return SWIGLU_ERR_ALIAS;
-    } else {
-        if (overlaps(sdxs, sxs) || overlaps(sdxs, sdys)) return SWIGLU_ERR_ALIAS;
-    }
+    if (overlaps(sxs, sys) || overlaps(sws, sys)) return SWIGLU_ERR_ALIAS;
     const char *xb = static_cast<const char *>(x);
-    char *dxb = static_cast<char *>(dx);
-    BwdArgs a{{dy, dy_row_stride},
-              {x, x_row_stride},
-              {xb + n * eb, x_row_stride},
-              {dx, dx_row_stride},
-              {dxb + n * eb, dx_row_stride},
-              rows,
-              n};
+    FwdArgs a{{x, x_row_stride}, {xb + n * eb, x_row_stride}, {y, y_row_stride}, rows, n};
+    a.mode = swiglu::kWeight;
+    a.w = w;
+    return run_fwd(dtype, a, stream);
+}
+
+swiglu_status_t swiglu_gateup_weighted_bwd(const void *dy, const void *x, const float *w, void *dx,
+                                           float *dw, int64_t rows, int64_t n,
+                                           int64_t dy_row_stride, int64_t x_row_stride,
+                                           int64_t dx_row_stride, swiglu_dtype_t dtype,
+                                           int in_place, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0) return SWIGLU_OK;
+    if (w == nullptr || dw == nullptr) return SWIGLU_ERR_NULL;
+    Span sws, sdws;
+    if (!span_of(w, 1, rows, rows, 4, sws) || !span_of(dw, 1, rows, rows, 4, sdws))
+        return SWIGLU_ERR_SHAPE;
+    if (overlaps(sws, sdws)) return SWIGLU_ERR_ALIAS;
+    if (n == 0) {  // every row sums nothing
+        cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)rows * sizeof(float),
+                                        reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+    }
+    BwdArgs a;
+    Span sp[3];
+    st = gateup_bwd_args(dy, x, dx, rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
+                         in_place, a, sp);
+    if (st != SWIGLU_OK) return st;
+    // dw may overlap nothing; w may not overlap the written dx
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(sdws, sp[i])) return SWIGLU_ERR_ALIAS;
+    if (overlaps(sws, sp[2])) return SWIGLU_ERR_ALIAS;
+    a.mode = swiglu::kWeight;
+    a.w = w;
+    a.dw = dw;
+    return run_bwd(dtype, in_place != 0, a, stream);
+}
+
+swiglu_status_t swiglu_gateup_bias_fwd(const void *x, const void *bias, void *y, int64_t rows,
+                                       int64_t n, int64_t x_row_stride, int64_t y_row_stride,
+                                       swiglu_dtype_t dtype, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
+    if (x == nullptr || y == nullptr || bias == nullptr) return SWIGLU_ERR_NULL;
+    if (x_row_stride < 2 * n || y_row_stride < n) return SWIGLU_ERR_STRIDE;
+    Span sxs, sys, sbs;
+    if (!span_of(x, rows, 2 * n, x_row_stride, eb, sxs) ||
+        !span_of(y, rows, n, y_row_stride, eb, sys) || !span_of(bias, 1, 2 * n, 2 * n, eb, sbs))
+        return SWIGLU_ERR_SHAPE;
+    if (overlaps(sxs, sys) || overlaps(sbs, sys)) return SWIGLU_ERR_ALIAS;
+    const char *xb = static_cast<const char *>(x);
+    FwdArgs a{{x, x_row_stride}, {xb + n * eb, x_row_stride}, {y, y_row_stride}, rows, n};
+    a.mode = swiglu::kBias;
+    a.bias_g = bias;
+    a.bias_u = static_cast<const char *>(bias) + n * eb;
+    return run_fwd(dtype, a, stream);
+}
+
+swiglu_status_t swiglu_gateup_bias_bwd_workspace_size(int64_t rows, int64_t n, size_t *bytes) {
+    if (bytes == nullptr) return SWIGLU_ERR_NULL;
+    if (rows < 0 || n < 0 || n > SWIGLU_MAX_N) return SWIGLU_ERR_SHAPE;
+    *bytes = 0;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *bytes = bias_plan(rows, n, d.sms).workspace_bytes;
+    return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void *bias, void *dx,
+                                       void *dbias, void *workspace, size_t workspace_bytes,
+                                       int64_t rows, int64_t n, int64_t dy_row_stride,
+                                       int64_t x_row_stride, int64_t dx_row_stride,
+                                       swiglu_dtype_t dtype, int in_place,
+                                       swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (n == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
+    if (bias == nullptr || dbias == nullptr) return SWIGLU_ERR_NULL;
+    Span sbs, sdbs;
+    if (!span_of(bias, 1, 2 * n, 2 * n, eb, sbs) || !span_of(dbias, 1, 2 * n, 2 * n, eb, sdbs))
+        return SWIGLU_ERR_SHAPE;
+    if (overlaps(sbs, sdbs)) return SWIGLU_ERR_ALIAS;
+    if (rows == 0) {  // the sum over no rows
+        cudaError_t e = cudaMemsetAsync(dbias, 0, (size_t)(2 * n) * eb,
+                                        reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+    }
+    if (workspace == nullptr) return SWIGLU_ERR_NULL;
+    BwdArgs a;
+    Span sp[3];
+    st = gateup_bwd_args(dy, x, dx, rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
+                         in_place, a, sp);
+    if (st != SWIGLU_OK) return st;
+    Span sws;
+    if (!span_of(workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1, sws))
+        return SWIGLU_ERR_SHAPE;
+    // dbias and the workspace are written: they overlap nothing; bias is read
+    // while dx is written
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(sdbs, sp[i]) || overlaps(sws, sp[i])) return SWIGLU_ERR_ALIAS;
+    if (overlaps(sws, sbs) || overlaps(sws, sdbs) || overlaps(sbs, sp[2])) return SWIGLU_ERR_ALIAS;
+    if ((uintptr_t)workspace % 16 != 0) return SWIGLU_ERR_WORKSPACE;
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (workspace_bytes < bias_plan(rows, n, d.sms).workspace_bytes) return SWIGLU_ERR_WORKSPACE;
+    a.mode = swiglu::kBias;
+    a.bias_g = bias;
+    a.bias_u = static_cast<const char *>(bias) + n * eb;
+    a.dbias = dbias;
+    a.partial = static_cast<float *>(workspace);
     return run_bwd(dtype, in_place != 0, a, stream);
 }
 
@@ -391,12 +640,13 @@ const char *swiglu_status_string(swiglu_status_t status) {
         case SWIGLU_ERR_STRIDE: return "row stride shorter than the row (or in-place stride mismatch)";
         case SWIGLU_ERR_ALIAS: return "output overlaps an input it must not overlap";
         case SWIGLU_ERR_CUDA: return "CUDA runtime error (see swiglu_last_cuda_error)";
+        case SWIGLU_ERR_WORKSPACE: return "workspace too small or not 16-byte aligned";
     }
     return "unknown status";
 }
 
 int swiglu_last_cuda_error(void) { return g_last_cuda_error; }
 
-int swiglu_abi_version(void) { return 2; }
+int swiglu_abi_version(void) { return 3; }
 
 }  // extern "C"

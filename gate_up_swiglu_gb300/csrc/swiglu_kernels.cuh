@@ -36,12 +36,14 @@ constexpr int kThreads = 256;
 //           kLdNoAlloc256  ... .L2::256B           + 256-byte L2 prefetch
 //           kLdNC          ld.global.nc.L1::no_allocate   read-only path
 //           kLdNC256       ... .L2::256B           + 256-byte L2 prefetch
+//           kLdCached      ld.global.nc            read-only, cached in L1 (bias
+//                                                  vectors reread by every row)
 //   stores  kStStream      st.global.cs            evict-first
 //           kStNoAlloc     st.global.L1::no_allocate
 //           kStPlain       st.global
 // The read-only (.nc) kinds are only legal when no thread of the kernel writes
 // the loaded memory, i.e. never for the in-place backward.
-enum : int { kLdStream = 0, kLdNoAlloc = 1, kLdNoAlloc256 = 2, kLdNC = 3, kLdNC256 = 4 };
+enum : int { kLdStream = 0, kLdNoAlloc = 1, kLdNoAlloc256 = 2, kLdNC = 3, kLdNC256 = 4, kLdCached = 5 };
 enum : int { kStStream = 0, kStNoAlloc = 1, kStPlain = 2 };
 
 template <int B, int KIND>
@@ -93,6 +95,7 @@ SWIGLU_DEFINE_LD(kLdNoAlloc, "ld.global.L1::no_allocate")
 SWIGLU_DEFINE_LD(kLdNoAlloc256, "ld.global.L1::no_allocate.L2::256B")
 SWIGLU_DEFINE_LD(kLdNC, "ld.global.nc.L1::no_allocate")
 SWIGLU_DEFINE_LD(kLdNC256, "ld.global.nc.L1::no_allocate.L2::256B")
+SWIGLU_DEFINE_LD(kLdCached, "ld.global.nc")
 #undef SWIGLU_DEFINE_LD
 
 #define SWIGLU_DEFINE_ST(KIND, QUAL)                                                           \
@@ -286,10 +289,19 @@ __device__ __forceinline__ void store_pack(uint32_t *w, const float *v) {
 // The gate and up operands are addressed separately (base pointer and row
 // stride each), which covers both the fused [rows, 2n] buffer (up = gate + n,
 // same stride) and two separate tensors.
+// Variants of the activation:
+//   kPlain   silu(g) * u
+//   kBias    silu(g + bias_g[j]) * (u + bias_u[j])
+//   kWeight  w[r] * silu(g) * u            (w: fp32 per row)
+enum : int { kPlain = 0, kBias = 1, kWeight = 2 };
+
 struct FwdParams {
     const void *g;
     const void *u;
     void *y;
+    const void *bias_g;  // kBias: [n] bias of the gate half
+    const void *bias_u;  // kBias: [n] bias of the up half
+    const float *w;      // kWeight: [rows]
     int64_t rows;
     int64_t g_stride;  // row strides, in packs
     int64_t u_stride;
@@ -305,6 +317,11 @@ struct BwdParams {
     const void *u;
     void *dg;  // == g for the in-place backward
     void *du;  // == u for the in-place backward
+    const void *bias_g;  // kBias
+    const void *bias_u;
+    const float *w;      // kWeight: [rows]
+    float *dw;           // kWeight: [rows]
+    float *partial;      // kBias: [groups, 2n] fp32 column sums per row group
     int64_t rows;
     int64_t dy_stride;  // row strides, in packs
     int64_t g_stride;
@@ -341,7 +358,7 @@ __device__ __forceinline__ void advance(int64_t step_q, int32_t step_r, int32_t 
     }
 }
 
-template <typename E, int VEC, int U, int LD, int ST>
+template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain>
 __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
@@ -356,11 +373,18 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
     first_positions<U>(p.nvec, r, c);
     while (r[0] < p.rows) {
         uint32_t g[U][NW], u[U][NW];
+        uint32_t bg[U][NW], bu[U][NW];
+        float wr[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (r[k] < p.rows) {
                 L::run(gp + (r[k] * p.g_stride + c[k]) * B, g[k]);
                 L::run(up + (r[k] * p.u_stride + c[k]) * B, u[k]);
+                if (MODE == kBias) {
+                    Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_g) + (int64_t)c[k] * B, bg[k]);
+                    Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_u) + (int64_t)c[k] * B, bu[k]);
+                }
+                if (MODE == kWeight) wr[k] = __ldg(p.w + r[k]);
             }
         }
 #pragma unroll
@@ -370,8 +394,15 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
                 float yv[VEC];
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
-                    const Act act = activation<E, false>(E::get(g[k], i));
-                    yv[i] = __fmul_rn(__fmul_rn(act.silu, E::get(u[k], i)), act.scale);
+                    float gf = E::get(g[k], i), uf = E::get(u[k], i);
+                    if (MODE == kBias) {
+                        gf = __fadd_rn(gf, E::get(bg[k], i));
+                        uf = __fadd_rn(uf, E::get(bu[k], i));
+                    }
+                    const Act act = activation<E, false>(gf);
+                    float v = __fmul_rn(act.silu, uf);
+                    if (MODE == kWeight) v = __fmul_rn(v, wr[k]);
+                    yv[i] = __fmul_rn(v, act.scale);
                 }
                 store_pack<E, VEC>(o, yv);
                 S::run(y + (r[k] * p.y_stride + c[k]) * B, o);
@@ -432,6 +463,206 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
             }
         }
         advance<U>(p.step_q, p.step_r, p.nvec, r, c);
+    }
+}
+
+// ------------------------------------------------ backward with reductions ---
+
+// Sum of v over the CTA (kThreads threads), in a fixed order; every thread
+// gets the result.  `red` is shared scratch of kThreads / 32 floats.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red may still be read from the previous call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kThreads / 32; ++k) t = __fadd_rn(t, red[k]);
+    return t;
+}
+
+// One element pair of the backward: dy scaled by the row weight when there is
+// one, gate and up shifted by their bias when there is one.
+template <typename E, int MODE>
+struct BwdPair {
+    float dg, du, dw_term;
+};
+
+template <typename E, int MODE>
+__device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float uf, float bgf,
+                                                     float buf, float wr) {
+    if (MODE == kBias) {
+        gf = __fadd_rn(gf, bgf);
+        uf = __fadd_rn(uf, buf);
+    }
+    const Act act = activation<E, true>(gf);
+    BwdPair<E, MODE> o;
+    o.dw_term = 0.0f;
+    if (MODE == kWeight) {
+        // dw[r] sums dy * silu(g) * u over the row; dy * w drives the gradient
+        o.dw_term = __fmul_rn(__fmul_rn(__fmul_rn(df, act.silu), uf), act.scale);
+        df = __fmul_rn(df, wr);
+    }
+    o.dg = __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale);
+    o.du = __fmul_rn(__fmul_rn(df, act.silu), act.scale);
+    return o;
+}
+
+// Weighted backward: one CTA per row (persistent over rows), so dw[r] is a
+// fixed-order reduction inside the CTA: no scratch, deterministic.
+template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
+__global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const BwdParams p) {
+    static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
+    constexpr int B = E::kBytes * VEC;
+    constexpr int NW = (B + 3) / 4;
+    using L = Ld<B, LD>;
+    using S = St<B, ST>;
+    __shared__ float red[kThreads / 32];
+    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+        const char *dyr = static_cast<const char *>(p.dy) + r * p.dy_stride * B;
+        const char *gr = static_cast<const char *>(p.g) + r * p.g_stride * B;
+        const char *ur = static_cast<const char *>(p.u) + r * p.u_stride * B;
+        char *dgr = static_cast<char *>(p.dg) + r * p.dg_stride * B;
+        char *dur = static_cast<char *>(p.du) + r * p.du_stride * B;
+        const float wr = __ldg(p.w + r);
+        float acc = 0.0f;
+        for (int32_t c0 = threadIdx.x; c0 < p.nvec; c0 += U * kThreads) {
+            uint32_t d[U][NW], g[U][NW], u[U][NW];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int32_t c = c0 + k * kThreads;
+                if (c < p.nvec) {
+                    L::run(dyr + (int64_t)c * B, d[k]);
+                    L::run(gr + (int64_t)c * B, g[k]);
+                    L::run(ur + (int64_t)c * B, u[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int32_t c = c0 + k * kThreads;
+                if (c < p.nvec) {
+                    uint32_t og[NW] = {}, ou[NW] = {};
+                    float gv[VEC], uv[VEC];
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        const BwdPair<E, kWeight> o = bwd_pair<E, kWeight>(
+                            E::get(d[k], i), E::get(g[k], i), E::get(u[k], i), 0.0f, 0.0f, wr);
+                        acc = __fadd_rn(acc, o.dw_term);
+                        gv[i] = o.dg;
+                        uv[i] = o.du;
+                    }
+                    store_pack<E, VEC>(og, gv);
+                    store_pack<E, VEC>(ou, uv);
+                    S::run(dgr + (int64_t)c * B, og);
+                    S::run(dur + (int64_t)c * B, ou);
+                }
+            }
+        }
+        acc = block_sum(acc, red);
+        if (threadIdx.x == 0) p.dw[r] = acc;
+    }
+}
+
+// Bias backward, first pass: CTA (tile, group) covers kBiasTileCols columns of
+// each half for the rows of its row group, writes dx and leaves the column
+// sums of its rows, in fp32, in partial[group][0, 2n).
+constexpr int kBiasTileCols = 2048;
+
+template <typename E, int VEC, bool IN_PLACE, int LD, int ST>
+__global__ void __launch_bounds__(kThreads) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
+                                                                   int64_t rows_per_group) {
+    static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
+    constexpr int B = E::kBytes * VEC;
+    constexpr int NW = (B + 3) / 4;
+    constexpr int PPT = kBiasTileCols / (kThreads * VEC);  // packs per thread per row and half
+    static_assert(PPT >= 1 && PPT * kThreads * VEC == kBiasTileCols, "tile / pack mismatch");
+    using L = Ld<B, LD>;
+    using S = St<B, ST>;
+    const int32_t tile = blockIdx.x % tiles;
+    const int64_t group = blockIdx.x / tiles;
+    const int64_t r0 = group * rows_per_group;
+    const int64_t r1 = min(p.rows, r0 + rows_per_group);
+    int32_t c[PPT];
+    float bg[PPT][VEC], bu[PPT][VEC], ag[PPT][VEC], au[PPT][VEC];
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        c[k] = tile * (kBiasTileCols / VEC) + k * kThreads + threadIdx.x;
+        uint32_t wb[NW], wu[NW];
+        if (c[k] < p.nvec) {
+            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_g) + (int64_t)c[k] * B, wb);
+            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_u) + (int64_t)c[k] * B, wu);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                bg[k][i] = E::get(wb, i);
+                bu[k][i] = E::get(wu, i);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
+    }
+    for (int64_t r = r0; r < r1; ++r) {
+        uint32_t d[PPT][NW], g[PPT][NW], u[PPT][NW];
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            if (c[k] < p.nvec) {
+                L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[k]);
+                L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[k]);
+                L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            if (c[k] < p.nvec) {
+                uint32_t og[NW] = {}, ou[NW] = {};
+                float gv[VEC], uv[VEC];
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    const BwdPair<E, kBias> o = bwd_pair<E, kBias>(
+                        E::get(d[k], i), E::get(g[k], i), E::get(u[k], i), bg[k][i], bu[k][i], 1.0f);
+                    ag[k][i] = __fadd_rn(ag[k][i], o.dg);
+                    au[k][i] = __fadd_rn(au[k][i], o.du);
+                    gv[i] = o.dg;
+                    uv[i] = o.du;
+                }
+                store_pack<E, VEC>(og, gv);
+                store_pack<E, VEC>(ou, uv);
+                S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
+                S::run(static_cast<char *>(p.du) + (r * p.du_stride + c[k]) * B, ou);
+            }
+        }
+    }
+    const int64_t n = (int64_t)p.nvec * VEC;
+    float *part = p.partial + group * 2 * n;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        if (c[k] < p.nvec) {
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                part[(int64_t)c[k] * VEC + i] = ag[k][i];
+                part[n + (int64_t)c[k] * VEC + i] = au[k][i];
+            }
+        }
+    }
+}
+
+// Bias backward, second pass: dbias[k] = sum over groups of partial[group][k],
+// in group order, rounded once to the storage type.
+template <typename E>
+__global__ void __launch_bounds__(kThreads) swiglu_bias_reduce_kernel(const float *partial,
+                                                                      int64_t groups, int64_t two_n,
+                                                                      void *dbias) {
+    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < two_n;
+         k += (int64_t)gridDim.x * kThreads) {
+        float s = 0.0f;
+        for (int64_t q = 0; q < groups; ++q) s = __fadd_rn(s, partial[q * two_n + k]);
+        uint32_t w[1] = {0};
+        E::put(w, 0, s);
+        if (E::kBytes == 4)
+            static_cast<uint32_t *>(dbias)[k] = w[0];
+        else
+            static_cast<unsigned short *>(dbias)[k] = (unsigned short)w[0];
     }
 }
 

@@ -17,7 +17,8 @@
  * The backward recomputes the sigmoid from the saved fc1 buffer and may write
  * its result over that buffer (§Optional: in_place=True).  The page prints no
  * backward formula; the one above is the analytic derivative of silu(g) * u.
- * bias is not supported (§Scope: bias=None).
+ * The plain entry points take no bias (§Scope: bias=None); the bias and
+ * per-token-weight variants further down are the page's named follow-ups.
  *
  * Conventions shared by every entry point:
  *   - All pointers are DEVICE pointers owned by the caller.  The library never
@@ -37,6 +38,7 @@
 #ifndef LIBSWIGLU_SWIGLU_H
 #define LIBSWIGLU_SWIGLU_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -60,8 +62,10 @@ typedef enum {
                                byte extent of a tensor overflows int64          */
     SWIGLU_ERR_STRIDE = -4, /* a row stride is shorter than its row             */
     SWIGLU_ERR_ALIAS = -5,  /* an output overlaps an input it must not overlap  */
-    SWIGLU_ERR_CUDA = -6    /* the CUDA runtime reported an error; see
+    SWIGLU_ERR_CUDA = -6,   /* the CUDA runtime reported an error; see
                                swiglu_last_cuda_error()                         */
+    SWIGLU_ERR_WORKSPACE = -7 /* workspace smaller than required, or not
+                                 16-byte aligned                                */
 } swiglu_status_t;
 
 /* Largest supported n (columns per half). */
@@ -123,6 +127,56 @@ swiglu_status_t swiglu_silu_mul_bwd(const void *dc, const void *a, const void *b
                                     int64_t a_row_stride, int64_t b_row_stride,
                                     int64_t da_row_stride, int64_t db_row_stride,
                                     swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+/*
+ * Per-token weights (Liger-Kernel Megatron SwiGLU page, §Known issues 2: MoE
+ * routed experts scale each token's activation by its routing weight and need a
+ * per_token_scale-aware kernel).  w and dw are fp32 vectors of `rows` floats
+ * (unit stride); everything else is as in swiglu_gateup_fwd / _bwd.
+ *   forward   y[r, j]  = w[r] * silu(g) * u
+ *   backward  dx       = the plain backward with dy[r, :] scaled by w[r]
+ *             dw[r]    = sum_j dy[r, j] * silu(g[r, j]) * u[r, j]   (fp32)
+ * y / dx / dw may not overlap w; dw may overlap nothing.  dw[r] is summed in
+ * fp32 in a fixed order (deterministic).  With n == 0 the backward sets dw to
+ * zero.
+ */
+swiglu_status_t swiglu_gateup_weighted_fwd(const void *x, const float *w, void *y, int64_t rows,
+                                           int64_t n, int64_t x_row_stride, int64_t y_row_stride,
+                                           swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+swiglu_status_t swiglu_gateup_weighted_bwd(const void *dy, const void *x, const float *w, void *dx,
+                                           float *dw, int64_t rows, int64_t n,
+                                           int64_t dy_row_stride, int64_t x_row_stride,
+                                           int64_t dx_row_stride, swiglu_dtype_t dtype,
+                                           int in_place, swiglu_stream_t stream);
+
+/*
+ * Bias (Liger-Kernel Megatron SwiGLU page, §Scope: Megatron's bias_swiglu_impl
+ * adds a [2n] bias before the activation; the page's kernels fall back when a
+ * bias is given).  bias and dbias are contiguous [2n] vectors of x's dtype:
+ *   forward   y[r, j]  = silu(g + bias[j]) * (u + bias[n + j])
+ *   backward  dx       = the plain backward at (g + bias[j], u + bias[n + j])
+ *             dbias[k] = sum_r dx[r, k] for k < 2n (fp32 sum of the unrounded
+ *                        fp32 gradients, rounded once; fixed order)
+ * The backward needs a caller-provided device workspace of at least
+ * swiglu_gateup_bias_bwd_workspace_size(rows, n) bytes, 16-byte aligned; it
+ * holds per-row-group column sums and is overwritten (no state survives the
+ * call).  The size depends on the current device's SM count.  y / dx / dbias
+ * / workspace may not overlap bias, and dbias and the workspace overlap
+ * nothing.  With rows == 0 (and n > 0) the backward sets dbias to zero.
+ */
+swiglu_status_t swiglu_gateup_bias_fwd(const void *x, const void *bias, void *y, int64_t rows,
+                                       int64_t n, int64_t x_row_stride, int64_t y_row_stride,
+                                       swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+swiglu_status_t swiglu_gateup_bias_bwd_workspace_size(int64_t rows, int64_t n, size_t *bytes);
+
+swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void *bias, void *dx,
+                                       void *dbias, void *workspace, size_t workspace_bytes,
+                                       int64_t rows, int64_t n, int64_t dy_row_stride,
+                                       int64_t x_row_stride, int64_t dx_row_stride,
+                                       swiglu_dtype_t dtype, int in_place,
+                                       swiglu_stream_t stream);
 
 /* Static English text for a status code; never NULL. */
 const char *swiglu_status_string(swiglu_status_t status);

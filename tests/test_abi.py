@@ -33,6 +33,8 @@ def declared_functions():
 def test_header_declares_expected_calls():
     assert declared_functions() == sorted(
         ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
+         "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
+         "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
          "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
 
 
@@ -49,11 +51,11 @@ def test_library_exports_every_declared_symbol(sw):
 
 
 def test_status_strings(sw):
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         s = sw.status_string(code)
         assert s and s != "unknown status"
     assert sw.status_string(-99) == "unknown status"
-    assert sw.lib.swiglu_abi_version() == 2
+    assert sw.lib.swiglu_abi_version() == 3
     assert sw.lib.swiglu_last_cuda_error() == 0
 
 
@@ -143,6 +145,54 @@ def test_two_tensor_rejections(sw):
     # da partially over a is rejected; exactly a (same stride) is the in-place form
     assert mbwd(sw, da=A + 2) == -5
     assert mbwd(sw, da=A, s=(8, 8, 8, 16, 8)) == -5
+
+
+W, DW, BIAS, DBIAS, WS = 0x60_0000_0000, 0x70_0000_0000, 0x80_0000_0000, 0x90_0000_0000, 0xA0_0000_0000
+
+
+def test_weighted_rejections(sw):
+    f = lambda **k: sw.lib.swiglu_gateup_weighted_fwd(  # noqa: E731
+        k.get("x", X), k.get("w", W), k.get("y", Y), k.get("rows", 4), 8, 16, 8, BF16, None)
+    b = lambda **k: sw.lib.swiglu_gateup_weighted_bwd(  # noqa: E731
+        DY, X, k.get("w", W), k.get("dx", DX), k.get("dw", DW), k.get("rows", 4), k.get("n", 8),
+        8, 16, 16, BF16, k.get("ip", 0), None)
+    assert f(w=None) == -1
+    assert f(rows=-1) == -3
+    assert f(y=W - 4) == -5          # y over w
+    assert b(rows=0, w=None) == 0
+    assert b(dw=None) == -1
+    assert b(w=None) == -1
+    assert b(dw=W + 4) == -5         # dw over w
+    assert b(dw=X + 8) == -5         # dw over x
+    assert b(dw=DX + 8) == -5        # dw over dx
+    assert b(w=DX) == -5             # w under the written dx
+    assert b(ip=1, dx=DX) == -5      # the in-place contract still holds
+
+
+def test_bias_rejections(sw):
+    import ctypes
+
+    out = ctypes.c_size_t(123)
+    assert sw.lib.swiglu_gateup_bias_bwd_workspace_size(0, 8, ctypes.byref(out)) == 0
+    assert out.value == 0
+    assert sw.lib.swiglu_gateup_bias_bwd_workspace_size(-1, 8, ctypes.byref(out)) == -3
+    assert sw.lib.swiglu_gateup_bias_bwd_workspace_size(4, 8, None) == -1
+    f = lambda **k: sw.lib.swiglu_gateup_bias_fwd(  # noqa: E731
+        X, k.get("bias", BIAS), k.get("y", Y), 4, 8, 16, 8, BF16, None)
+    assert f(bias=None) == -1
+    assert f(y=BIAS + 4) == -5
+    b = lambda **k: sw.lib.swiglu_gateup_bias_bwd(  # noqa: E731
+        DY, X, k.get("bias", BIAS), k.get("dx", DX), k.get("dbias", DBIAS), k.get("ws", WS),
+        k.get("wsb", 1 << 20), k.get("rows", 4), 8, 8, 16, 16, BF16, k.get("ip", 0), None)
+    assert b(bias=None) == -1
+    assert b(dbias=None) == -1
+    assert b(ws=None) == -1
+    assert b(dbias=BIAS + 2) == -5       # dbias over bias
+    assert b(dbias=X + 2) == -5          # dbias over x
+    assert b(ws=DX + 16) == -5           # workspace over dx
+    assert b(ws=BIAS) == -5              # workspace over bias
+    assert b(bias=DX) == -5              # bias under the written dx
+    assert b(ws=WS + 4) == -7            # misaligned workspace
 
 
 def test_import_fails_loudly_without_the_library(tmp_path):

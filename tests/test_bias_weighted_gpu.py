@@ -1,0 +1,180 @@
+"""Per-token-weighted and bias variants vs the oracle, through the C ABI.
+
+Elementwise outputs (y, dx) use the tolerances of tests/helpers.py.  The two
+reductions -- dw[r] (a sum over the n columns of a row) and dbias[k] (a sum
+over the rows of a column) -- are fp32 sums in a fixed order, so they are held
+to the rigorous bound of such a sum: with A = sum |t| over the exact terms and
+D the summation depth of the kernel (terms added one after another along the
+longest chain),
+    |gpu - exact| <= (D + 6) * 2^-24 * A  +  one step of the output type at |exact|.
+For dw, D = n / 256 (the columns one thread adds) + 5 (warp shuffle levels) +
+8 (warp partials).  For dbias, D = rows per row group + number of groups,
+from the same plan the library makes (2048-column tiles, 3 CTAs per SM).
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import assert_bitwise, assert_parity
+
+pytestmark = pytest.mark.gpu
+U32 = 2.0 ** -24
+
+
+@pytest.fixture(scope="module")
+def sw():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from conftest import build_library
+
+    build_library()
+    import gate_up_swiglu_gb300 as sw
+
+    return sw
+
+
+def _step(dtype, mag: torch.Tensor) -> torch.Tensor:
+    """One step of `dtype` at magnitude mag (subnormal steps included)."""
+    mant = 7 if dtype == torch.bfloat16 else 23
+    return torch.clamp(mag, min=2.0 ** -126) * 2.0 ** -mant
+
+
+def assert_reduction(gpu, exact, abs_sum, depth, what):
+    dtype = gpu.dtype
+    gpu = gpu.cpu().double()
+    bound = (depth + 6) * U32 * abs_sum
+    tol = bound + _step(dtype, exact.abs() + bound)
+    bad = (gpu - exact).abs() > tol
+    nb = int(bad.sum())
+    if nb:
+        i = bad.nonzero()[:5].flatten().tolist()
+        raise AssertionError(f"{what}: {nb} of {gpu.numel()} sums out of bound; first: "
+                             f"{[(k, float(gpu[k]), float(exact[k]), float(tol[k])) for k in i]}")
+
+
+def _bias_depth(rows, n):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-n // 2048)
+    groups = max(1, min(rows, (sms * 3) // tiles))
+    rpg = -(-rows // groups)
+    groups = -(-rows // rpg)
+    return rpg + groups
+
+
+CASES = [("tiny_f32", None), ("megatron_4096_bf16", 300), ("odd_5503_f32", 97),
+         ("llama_14336_bf16_2d", 64)]
+
+
+@pytest.mark.parametrize("name,rows", CASES)
+def test_weighted_matches_oracle(sw, name, rows):
+    w_ = W.WORKLOADS[name]
+    x, dy = W.make_inputs(w_, "cpu", rows=rows)
+    r = x.shape[0]
+    g = torch.Generator().manual_seed(5)
+    wts = torch.rand(r, generator=g)  # routing weights in [0, 1)
+    xd, dyd, wd = x.cuda(), dy.cuda(), wts.cuda()
+    y = sw.swiglu_gateup_weighted_fwd(xd, wd)
+    dx, dw = sw.swiglu_gateup_weighted_bwd(dyd, xd, wd)
+    xi = xd.clone()
+    dxi, dwi = sw.swiglu_gateup_weighted_bwd(dyd, xi, wd, in_place=True)
+    torch.cuda.synchronize()
+    assert_parity(y, oracle.weighted_fwd(x, wts), f"{name} weighted fwd")
+    rdx, _ = oracle.weighted_bwd(dy, x, wts)
+    assert_parity(dx, rdx, f"{name} weighted dx")
+    assert_bitwise(xi, dx, "weighted in-place dx")
+    assert_bitwise(dwi, dw, "weighted in-place dw")
+    # exact dw and |terms| from the fp64 oracle on the same (exactly widened) values
+    x64, dy64 = x.double(), dy.double()
+    _, dw64 = oracle.weighted_bwd(dy64, x64, wts)  # dw is returned rounded to fp32
+    terms = (dy64 * oracle.fwd(x64)).abs().sum(1)
+    exact = (dy64 * oracle.fwd(x64)).sum(1)
+    assert torch.allclose(dw64.double(), exact, rtol=1e-6, atol=1e-30)
+    assert_reduction(dw, exact, terms, w_.n / 256 + 13, f"{name} dw")
+
+
+@pytest.mark.parametrize("name,rows", CASES)
+def test_bias_matches_oracle(sw, name, rows):
+    w_ = W.WORKLOADS[name]
+    x, dy = W.make_inputs(w_, "cpu", rows=rows)
+    r, n = x.shape[0], w_.n
+    g = torch.Generator().manual_seed(6)
+    bias = (torch.randn(2 * n, generator=g) * 0.5).to(x.dtype)
+    xd, dyd, bd = x.cuda(), dy.cuda(), bias.cuda()
+    y = sw.swiglu_gateup_bias_fwd(xd, bd)
+    dx, db = sw.swiglu_gateup_bias_bwd(dyd, xd, bd)
+    xi = xd.clone()
+    dxi, dbi = sw.swiglu_gateup_bias_bwd(dyd, xi, bd, in_place=True)
+    torch.cuda.synchronize()
+    assert_parity(y, oracle.bias_fwd(x, bias), f"{name} bias fwd")
+    rdx, _ = oracle.bias_bwd(dy, x, bias)
+    assert_parity(dx, rdx, f"{name} bias dx")
+    assert_bitwise(xi, dx, "bias in-place dx")
+    assert_bitwise(dbi, db, "bias in-place dbias")
+    dx64, db64 = oracle.bias_bwd(dy.double(), x.double(), bias.double())
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(r, n), f"{name} dbias")
+
+
+def test_bias_full_size_columns(sw):
+    """Large-FFN workload at full size, the launch configuration of the bench:
+    dx on sampled rows, dbias on sampled columns (the oracle over all 8192 rows
+    of those columns)."""
+    w_ = W.WORKLOADS["large_32768_bf16"]
+    x, dy = W.make_inputs(w_, "cuda")
+    n = w_.n
+    g = torch.Generator().manual_seed(7)
+    bias = (torch.randn(2 * n, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    dx, db = sw.swiglu_gateup_bias_bwd(dy, x, bias)
+    y = sw.swiglu_gateup_bias_fwd(x, bias)
+    torch.cuda.synchronize()
+    rows_idx = torch.tensor([0, 1, 4097, 8190, 8191], device="cuda")
+    xs, dys = x[rows_idx].cpu(), dy[rows_idx].cpu()
+    assert_parity(y[rows_idx], oracle.bias_fwd(xs, bias.cpu()), "full bias fwd rows")
+    assert_parity(dx[rows_idx], oracle.bias_bwd(dys, xs, bias.cpu())[0], "full bias dx rows")
+    cols = torch.tensor(sorted(set([0, 1, 2047, 2048, n - 1] +
+                                   torch.randperm(n, generator=g)[:59].tolist())))
+    cc = cols.cuda()
+    xsub = torch.cat([x[:, cc], x[:, n + cc]], 1).cpu()
+    dysub = dy[:, cc].cpu()
+    bsub = torch.cat([bias[cc], bias[n + cc]]).cpu()
+    dx64, db64 = oracle.bias_bwd(dysub.double(), xsub.double(), bsub.double())
+    got = torch.cat([db[cc], db[n + cc]])
+    assert_reduction(got, db64, dx64.abs().sum(0), _bias_depth(w_.rows, n), "full dbias columns")
+
+
+def test_weighted_full_size_rows(sw):
+    w_ = W.WORKLOADS["large_32768_bf16"]
+    x, dy = W.make_inputs(w_, "cuda")
+    wts = torch.rand(w_.rows, generator=torch.Generator().manual_seed(8)).cuda()
+    y = sw.swiglu_gateup_weighted_fwd(x, wts)
+    dx, dw = sw.swiglu_gateup_weighted_bwd(dy, x, wts)
+    torch.cuda.synchronize()
+    idx = torch.tensor([0, 1, 3000, 8190, 8191], device="cuda")
+    xs, dys, ws = x[idx].cpu(), dy[idx].cpu(), wts[idx].cpu()
+    assert_parity(y[idx], oracle.weighted_fwd(xs, ws), "full weighted fwd rows")
+    assert_parity(dx[idx], oracle.weighted_bwd(dys, xs, ws)[0], "full weighted dx rows")
+    t = dys.double() * oracle.fwd(xs.double())
+    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), w_.n / 256 + 13, "full dw rows")
+
+
+def test_empty_and_workspace_errors(sw):
+    n = 64
+    bias = torch.randn(2 * n, device="cuda")
+    x = torch.empty(0, 2 * n, device="cuda")
+    dbias = torch.full((2 * n,), 7.0, device="cuda")
+    sw.swiglu_gateup_bias_bwd(torch.empty(0, n, device="cuda"), x, bias, dbias=dbias)
+    assert torch.equal(dbias, torch.zeros_like(dbias))  # the sum over no rows
+    x = torch.randn(32, 2 * n, device="cuda")
+    dy = torch.randn(32, n, device="cuda")
+    need = sw.bias_bwd_workspace_bytes(32, n)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sw.SwigluError) as e:
+        sw.swiglu_gateup_bias_bwd(dy, x, bias, workspace=small)
+    assert e.value.status == -7
+    dw = torch.full((32,), 3.0, device="cuda")
+    sw.swiglu_gateup_weighted_bwd(torch.empty(32, 0, device="cuda"), torch.empty(32, 0, device="cuda"),
+                                  torch.ones(32, device="cuda"), dw=dw)
+    assert torch.equal(dw, torch.zeros_like(dw))
