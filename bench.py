@@ -419,7 +419,39 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
         torch.autograd.grad(y, xs, dys)
 
     ag_ms = _event_ms(ag_step, stream, reps)
+    del xs
+
+    # per-token weights and bias on the same x / dy
+    g = torch.Generator().manual_seed(11)
+    wts = torch.rand(w.rows, generator=g).to(dev)
+    bias = (torch.randn(2 * n, generator=g) * 0.5).to(x.dtype).to(dev)
+    y = torch.empty((w.rows, n), dtype=x.dtype, device=dev)
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(wts)
+    dbias = torch.empty_like(bias)
+    ws = torch.empty(max(16, sw.bias_bwd_workspace_bytes(w.rows, n)), dtype=torch.uint8, device=dev)
+    wf = _event_ms(lambda: sw.swiglu_gateup_weighted_fwd(x, wts, y, stream=stream), stream, reps)
+    wb = _event_ms(lambda: sw.swiglu_gateup_weighted_bwd(dy, x, wts, dx, dw, stream=stream),
+                   stream, reps)
+    bf = _event_ms(lambda: sw.swiglu_gateup_bias_fwd(x, bias, y, stream=stream), stream, reps)
+    bb = _event_ms(lambda: sw.swiglu_gateup_bias_bwd(dy, x, bias, dx, dbias, ws, stream=stream),
+                   stream, reps)
+    del y, dx, dw, dbias
+
+    def row(f_ms, b_ms, extra_note):
+        return {"fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
+                "fwd_gbs": round(gbs(w.fwd_bytes(), f_ms), 1),
+                "bwd_gbs": round(gbs(w.bwd_bytes(), b_ms), 1),
+                "fwd_frac_of_measured": round(gbs(w.fwd_bytes(), f_ms) / peak, 4),
+                "bwd_frac_of_measured": round(gbs(w.bwd_bytes(), b_ms) / peak, 4),
+                "note": extra_note, "reps": reps}
+
     return {
+        "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "
+                                          "(one CTA per row); GB/s on the plain algorithmic bytes"),
+        "bias": row(bf, bb, f"[2n] bias; bwd includes the column-sum pass over a "
+                            f"{ws.numel() / 2**20:.1f} MiB workspace and the dbias reduction; "
+                            "GB/s on the plain algorithmic bytes"),
         "silu_mul_separate_tensors": {
             "layout": "gate and up as two contiguous [rows, n] tensors", "reps": reps,
             "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),

@@ -236,8 +236,20 @@ struct Act {
     float silu, dsilu, scale;
 };
 
+// Knuth's TwoSum: s = fl(a + b) and the exact rounding error e, a + b = s + e.
+__device__ __forceinline__ float two_sum(float a, float b, float &e) {
+    const float s = __fadd_rn(a, b);
+    const float bv = __fsub_rn(s, a);
+    const float av = __fsub_rn(s, bv);
+    e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+    return s;
+}
+
+// g_lo: a correction the exact gate value carries beyond the fp32 g (the
+// rounding error of g + bias); only the root window of silu' is sensitive
+// enough to need it.
 template <typename E, bool kGrad>
-__device__ __forceinline__ Act activation(float g) {
+__device__ __forceinline__ Act activation(float g, float g_lo = 0.0f) {
     const float a = fabsf(g);
     const bool pos = g >= 0.0f;
     // deep: for g < -64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or
@@ -261,7 +273,7 @@ __device__ __forceinline__ Act activation(float g) {
         const float oms = pos ? tr : r;
         o.dsilu = __fmul_rn(s, __fmaf_rn(g, oms, 1.0f));
         if (E::kRootWindow) {
-            const float d = __fsub_rn(__fsub_rn(g, SILU_ROOT_G0_HI), SILU_ROOT_G0_LO);
+            const float d = __fadd_rn(__fsub_rn(g, SILU_ROOT_G0_HI), __fsub_rn(g_lo, SILU_ROOT_G0_LO));
             if (fabsf(d) < SILU_ROOT_WINDOW) o.dsilu = dsilu_near_root(d);
         }
     }
@@ -493,11 +505,15 @@ struct BwdPair {
 template <typename E, int MODE>
 __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float uf, float bgf,
                                                      float buf, float wr) {
+    float g_lo = 0.0f;
     if (MODE == kBias) {
-        gf = __fadd_rn(gf, bgf);
+        if (E::kRootWindow)
+            gf = two_sum(gf, bgf, g_lo);
+        else
+            gf = __fadd_rn(gf, bgf);
         uf = __fadd_rn(uf, buf);
     }
-    const Act act = activation<E, true>(gf);
+    const Act act = activation<E, true>(gf, g_lo);
     BwdPair<E, MODE> o;
     o.dw_term = 0.0f;
     if (MODE == kWeight) {
