@@ -35,7 +35,7 @@ STATUS = {0: "SWIGLU_OK", -1: "SWIGLU_ERR_NULL", -2: "SWIGLU_ERR_DTYPE", -3: "SW
 EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
            "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-           "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
+           "swiglu_gateup_bias_bwd_noalloc", "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
 
 
 class SwigluError(RuntimeError):
@@ -71,6 +71,9 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_gateup_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i64, i64, i64,
                                            i64, i64, i32, i32, vp]
     lib.swiglu_gateup_bias_bwd.restype = i32
+    lib.swiglu_gateup_bias_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
+                                                   i32, vp]
+    lib.swiglu_gateup_bias_bwd_noalloc.restype = i32
     lib.swiglu_status_string.argtypes = [i32]
     lib.swiglu_status_string.restype = ctypes.c_char_p
     lib.swiglu_last_cuda_error.argtypes = []

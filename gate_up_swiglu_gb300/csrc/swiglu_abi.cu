@@ -650,3 +650,52 @@ int swiglu_last_cuda_error(void) { return g_last_cuda_error; }
 int swiglu_abi_version(void) { return 3; }
 
 }  // extern "C"
+
+// ------------------------------------------------ allocation-free variant ---
+// swiglu_gateup_bias_bwd_noalloc: the bias backward with its column-sum
+// scratch in a fixed file-scope device array instead of a caller workspace,
+// for callers that have no way to obtain device memory of their own.  Every
+// GPU that loads this library holds the array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SWIGLU_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on each device, looked up on the first
+// call made with that device current (host code cannot use the array's name
+// as a device address).
+std::atomic<void *> g_noalloc_addr[kMaxDevices];
+
+cudaError_t noalloc_scratch(int dev, void **out) {
+    void *p = (dev >= 0 && dev < kMaxDevices) ? g_noalloc_addr[dev].load() : nullptr;
+    if (p == nullptr) {
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) g_noalloc_addr[dev].store(p);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" swiglu_status_t swiglu_gateup_bias_bwd_noalloc(
+    const void *dy, const void *x, const void *bias, void *dx, void *dbias, int64_t rows, int64_t n,
+    int64_t dy_row_stride, int64_t x_row_stride, int64_t dx_row_stride, swiglu_dtype_t dtype,
+    int in_place, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (rows == 0 || n == 0)  // no scratch needed
+        return swiglu_gateup_bias_bwd(dy, x, bias, dx, dbias, nullptr, 0, rows, n, dy_row_stride,
+                                      x_row_stride, dx_row_stride, dtype, in_place, stream);
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (bias_plan(rows, n, d.sms).workspace_bytes > SWIGLU_NOALLOC_SCRATCH_BYTES)
+        return SWIGLU_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    e = noalloc_scratch(d.id, &scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return swiglu_gateup_bias_bwd(dy, x, bias, dx, dbias, scratch, SWIGLU_NOALLOC_SCRATCH_BYTES,
+                                  rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
+                                  in_place, stream);
+}

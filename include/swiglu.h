@@ -178,6 +178,40 @@ swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void
                                        swiglu_dtype_t dtype, int in_place,
                                        swiglu_stream_t stream);
 
+/*
+ * Allocation-free bias backward.  The page has no counterpart: this is an
+ * addition for callers that cannot hand the library any device memory -- for
+ * example code running under an engine that plans all device memory ahead of
+ * time and forbids allocation during a step, plugin interfaces whose host owns
+ * the allocator and exposes none to the plugin, or latency-bound paths that
+ * cannot afford cudaMalloc's implicit synchronisation.
+ *
+ * Same arguments, results and checks as swiglu_gateup_bias_bwd minus the
+ * workspace: the column-sum scratch lives in a fixed file-scope device array
+ * of SWIGLU_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - A problem whose scratch need (swiglu_gateup_bias_bwd_workspace_size)
+ *     exceeds SWIGLU_NOALLOC_SCRATCH_BYTES is rejected with
+ *     SWIGLU_ERR_WORKSPACE before anything is launched.  Need is about
+ *     3 * SMs * 2048 * 8 bytes when n is a multiple of 2048 (7 MiB on a 152-SM
+ *     GB300), more for ragged n, and 8 n bytes at least.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents (the
+ *     kernels overwrite every scratch value they later read, so nothing needs
+ *     to start at zero).  Calls that overlap on the GPU -- on different streams,
+ *     or from different threads without ordering -- race on it: serialise them.
+ */
+#define SWIGLU_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+swiglu_status_t swiglu_gateup_bias_bwd_noalloc(const void *dy, const void *x, const void *bias,
+                                               void *dx, void *dbias, int64_t rows, int64_t n,
+                                               int64_t dy_row_stride, int64_t x_row_stride,
+                                               int64_t dx_row_stride, swiglu_dtype_t dtype,
+                                               int in_place, swiglu_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 const char *swiglu_status_string(swiglu_status_t status);
 

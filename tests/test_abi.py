@@ -35,7 +35,7 @@ def test_header_declares_expected_calls():
         ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
          "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
          "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-         "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
+         "swiglu_gateup_bias_bwd_noalloc", "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
 
 
 def test_library_exports_every_declared_symbol(sw):
