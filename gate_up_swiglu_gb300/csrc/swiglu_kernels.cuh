@@ -587,13 +587,16 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const Bwd
 constexpr int kBiasTileCols = 2048;
 
 template <typename E, int VEC, bool IN_PLACE, int LD, int ST>
-__global__ void __launch_bounds__(kThreads) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
-                                                                   int64_t rows_per_group) {
+__global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
+                                                                      int64_t rows_per_group) {
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     constexpr int PPT = kBiasTileCols / (kThreads * VEC);  // packs per thread per row and half
     static_assert(PPT >= 1 && PPT * kThreads * VEC == kBiasTileCols, "tile / pack mismatch");
+    // rows whose loads are issued together: keeps about as many bytes in flight
+    // per thread as the streaming backward
+    constexpr int RU = PPT >= 2 ? 1 : 2;
     using L = Ld<B, LD>;
     using S = St<B, ST>;
     const int32_t tile = blockIdx.x % tiles;
@@ -618,34 +621,43 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_bias_kernel(const BwdPara
 #pragma unroll
         for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
     }
-    for (int64_t r = r0; r < r1; ++r) {
-        uint32_t d[PPT][NW], g[PPT][NW], u[PPT][NW];
+    for (int64_t rb = r0; rb < r1; rb += RU) {
+        uint32_t d[RU][PPT][NW], g[RU][PPT][NW], u[RU][PPT][NW];
 #pragma unroll
-        for (int k = 0; k < PPT; ++k) {
-            if (c[k] < p.nvec) {
-                L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[k]);
-                L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[k]);
-                L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[k]);
+        for (int q = 0; q < RU; ++q) {
+            const int64_t r = rb + q;
+#pragma unroll
+            for (int k = 0; k < PPT; ++k) {
+                if (r < r1 && c[k] < p.nvec) {
+                    L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[q][k]);
+                    L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[q][k]);
+                    L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[q][k]);
+                }
             }
         }
 #pragma unroll
-        for (int k = 0; k < PPT; ++k) {
-            if (c[k] < p.nvec) {
-                uint32_t og[NW] = {}, ou[NW] = {};
-                float gv[VEC], uv[VEC];
+        for (int q = 0; q < RU; ++q) {
+            const int64_t r = rb + q;
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const BwdPair<E, kBias> o = bwd_pair<E, kBias>(
-                        E::get(d[k], i), E::get(g[k], i), E::get(u[k], i), bg[k][i], bu[k][i], 1.0f);
-                    ag[k][i] = __fadd_rn(ag[k][i], o.dg);
-                    au[k][i] = __fadd_rn(au[k][i], o.du);
-                    gv[i] = o.dg;
-                    uv[i] = o.du;
+            for (int k = 0; k < PPT; ++k) {
+                if (r < r1 && c[k] < p.nvec) {
+                    uint32_t og[NW] = {}, ou[NW] = {};
+                    float gv[VEC], uv[VEC];
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        const BwdPair<E, kBias> o =
+                            bwd_pair<E, kBias>(E::get(d[q][k], i), E::get(g[q][k], i),
+                                               E::get(u[q][k], i), bg[k][i], bu[k][i], 1.0f);
+                        ag[k][i] = __fadd_rn(ag[k][i], o.dg);
+                        au[k][i] = __fadd_rn(au[k][i], o.du);
+                        gv[i] = o.dg;
+                        uv[i] = o.du;
+                    }
+                    store_pack<E, VEC>(og, gv);
+                    store_pack<E, VEC>(ou, uv);
+                    S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
+                    S::run(static_cast<char *>(p.du) + (r * p.du_stride + c[k]) * B, ou);
                 }
-                store_pack<E, VEC>(og, gv);
-                store_pack<E, VEC>(ou, uv);
-                S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
-                S::run(static_cast<char *>(p.du) + (r * p.du_stride + c[k]) * B, ou);
             }
         }
     }
