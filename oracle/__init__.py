@@ -77,6 +77,8 @@ def load(path: str = None):
         lib.oracle_swiglu_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                                ctypes.c_int]
         lib.oracle_swiglu_bias_bwd.restype = ctypes.c_int
+        lib.oracle_fc1_swiglu_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int]
+        lib.oracle_fc1_swiglu_fwd.restype = ctypes.c_int
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         if path is None:
@@ -229,6 +231,29 @@ def bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor, dx: torch.Te
     if rc != 0:
         raise ValueError("oracle_swiglu_bias_bwd rejected its arguments")
     return dx, dbias
+
+
+def fc1_swiglu_fwd(X: torch.Tensor, Wt: torch.Tensor, want_fc1: bool = False, lib=None):
+    """y = silu((X W^T)[:, :n]) * (X W^T)[:, n:] with W: [2n, K]; returns y, or
+    (y, fc1) with want_fc1.  Exact dot products, one rounding."""
+    lib = lib or load()
+    for t, nm in ((X, "X"), (Wt, "W")):
+        if t.device.type != "cpu" or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"oracle: {nm} must be a contiguous 2D CPU tensor")
+    M, K = X.shape
+    two_n, K2 = Wt.shape
+    if K2 != K or two_n % 2 or Wt.dtype != X.dtype:
+        raise ValueError("oracle: W must be [2n, K] with X's K and dtype")
+    n = two_n // 2
+    y = torch.empty((M, n), dtype=X.dtype)
+    fc1 = torch.empty((M, two_n), dtype=X.dtype) if want_fc1 else None
+    acc = torch.empty(two_n, dtype=torch.float64)
+    rc = lib.oracle_fc1_swiglu_fwd(X.data_ptr(), Wt.data_ptr(), y.data_ptr(),
+                                   fc1.data_ptr() if want_fc1 else None, acc.data_ptr(), M, n, K,
+                                   _CODE[X.dtype])
+    if rc != 0:
+        raise ValueError("oracle_fc1_swiglu_fwd rejected its arguments")
+    return (y, fc1) if want_fc1 else y
 
 
 def bf16_from_double(v: float, lib=None) -> int:

@@ -290,3 +290,35 @@ int oracle_swiglu_bias_bwd(const void *dy, const void *x, const void *bias, void
     for (int64_t k = 0; k < 2 * n; ++k) store_elem(dbias, k, dtype, acc[k]);
     return ORACLE_OK;
 }
+
+/* ---- linear_fc1 followed by the activation -------------------------------- */
+/* Liger-Kernel Megatron SwiGLU page, §Background: the [s, b, 2n] buffer is the
+ * output of Megatron's linear_fc1 (a ColumnParallelLinear), i.e. fc1 = X W^T with
+ * W the [2n, K] weight whose rows [0, n) produce the gate and [n, 2n) the up
+ * projection.  Stated plainly (bias-free, as the fused path requires):
+ *   fc1[m, c] = sum_k X[m, k] * W[c, k]        (c < 2n, exact sum in double)
+ *   y[m, j]   = silu(fc1[m, j]) * fc1[m, n + j]
+ * y is rounded once to the storage type; when x_out is not NULL the
+ * pre-activation fc1 is also returned (rounded once), as a training step saves
+ * it for the backward.  X: [M, K], W: [2n, K], both row-major with unit column
+ * stride; `acc` is caller scratch of 2n doubles. */
+int oracle_fc1_swiglu_fwd(const void *X, const void *W, void *y, void *x_out, double *acc,
+                          int64_t M, int64_t n, int64_t K, int dtype) {
+    if (check_args(M, n, dtype) || K < 0) return ORACLE_BAD_ARG;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t c = 0; c < 2 * n; ++c) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                s += load_elem(X, m * K + k, dtype) * load_elem(W, c * K + k, dtype);
+            acc[c] = s;
+        }
+        for (int64_t j = 0; j < n; ++j) {
+            store_elem(y, m * n + j, dtype, swiglu_fwd_pair(acc[j], acc[n + j]));
+            if (x_out != NULL) {
+                store_elem(x_out, m * 2 * n + j, dtype, acc[j]);
+                store_elem(x_out, m * 2 * n + n + j, dtype, acc[n + j]);
+            }
+        }
+    }
+    return ORACLE_OK;
+}

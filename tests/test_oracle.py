@@ -356,9 +356,28 @@ def pin_bias(lib):
                            torch.tensor([oracle.bf16_from_double(float(v), lib=lib) for v in db64]))
 
 
+def pin_fc1_swiglu(lib):
+    """linear_fc1 then the activation: equals torch float64 matmul X @ W.T
+    followed by F.silu(gate) * up, and its fc1 output equals that matmul; with
+    W = [I; I] (K = n) it reduces to the plain form on x = [X, X]."""
+    for seed, (M, n, K) in enumerate([(7, 5, 9), (3, 16, 64), (1, 1, 1)]):
+        X = _rand((M, K), 160 + seed)
+        Wt = _rand((2 * n, K), 170 + seed, 0.3)
+        y, fc1 = oracle.fc1_swiglu_fwd(X, Wt, want_fc1=True, lib=lib)
+        ref = X @ Wt.T
+        assert torch.allclose(fc1, ref, rtol=1e-12, atol=1e-14)
+        assert torch.allclose(y, F.silu(ref[:, :n]) * ref[:, n:], rtol=1e-12, atol=1e-14)
+    n = 6
+    X = _rand((4, n), 180)
+    Wt = torch.cat([torch.eye(n), torch.eye(n)]).double()
+    x2 = torch.cat([X, X], 1)
+    assert torch.equal(oracle.fc1_swiglu_fwd(X, Wt, lib=lib), oracle.fwd(x2, lib=lib))
+
+
 PINS = [pin_zero_gate, pin_saturation, pin_stationary_point, pin_finite_differences,
         pin_torch_two_tensor, pin_bf16_rounding_brute, pin_rounding_matches_torch,
-        pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form, pin_weighted, pin_bias]
+        pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form, pin_weighted, pin_bias,
+        pin_fc1_swiglu]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -398,6 +417,9 @@ MUTATIONS = {
     "weighted_grad_unscaled": ("swiglu_bwd_pair(d * wr, g, u, &dg, &du);", "swiglu_bwd_pair(d, g, u, &dg, &du);"),
     "bias_halves_swapped": ("double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);\n            store_elem(y",
                             "double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, j, dtype);\n            store_elem(y"),
+    "fc1_weight_transposed": ("load_elem(W, c * K + k, dtype)", "load_elem(W, k * 2 * n + c, dtype)"),
+    "fc1_halves_swapped": ("store_elem(y, m * n + j, dtype, swiglu_fwd_pair(acc[j], acc[n + j]));",
+                           "store_elem(y, m * n + j, dtype, swiglu_fwd_pair(acc[n + j], acc[j]));"),
     "dbias_last_row_only": ("            acc[j] += dg;\n            acc[n + j] += du;", "            acc[j] = dg;\n            acc[n + j] = du;"),
 }
 
