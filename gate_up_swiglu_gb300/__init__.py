@@ -35,7 +35,8 @@ STATUS = {0: "SWIGLU_OK", -1: "SWIGLU_ERR_NULL", -2: "SWIGLU_ERR_DTYPE", -3: "SW
 EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
            "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-           "swiglu_gateup_bias_bwd_noalloc", "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
+           "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
+           "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
 
 
 class SwigluError(RuntimeError):
@@ -74,6 +75,10 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_gateup_bias_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
                                                    i32, vp]
     lib.swiglu_gateup_bias_bwd_noalloc.restype = i32
+    lib.swiglu_fc1_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.swiglu_fc1_fwd.restype = i32
+    lib.swiglu_fc1_timeout_flag.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.swiglu_fc1_timeout_flag.restype = i32
     lib.swiglu_status_string.argtypes = [i32]
     lib.swiglu_status_string.restype = ctypes.c_char_p
     lib.swiglu_last_cuda_error.argtypes = []
@@ -326,7 +331,42 @@ def swiglu_gateup_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
     return dx, dbias
 
 
-__all__ = ["swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
+def swiglu_fc1_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor = None,
+                   x_out: torch.Tensor = None, return_fc1: bool = False, stream=None):
+    """y = silu((x W^T)[..., :n]) * (x W^T)[..., n:] on the tensor cores, with W
+    the [2n, K] fc1 weight.  With return_fc1 (or an x_out given) the bf16 fc1
+    output is stored too and (y, fc1) is returned."""
+    K = x.shape[-1]
+    if w.dim() != 2 or w.shape[1] != K or w.shape[0] % 2:
+        raise ValueError("w must be [2n, K] with x's K")
+    n = w.shape[0] // 2
+    M = x.numel() // K if K else 0
+    if y is None:
+        y = torch.empty((*x.shape[:-1], n), dtype=x.dtype, device=x.device)
+    if return_fc1 and x_out is None:
+        x_out = torch.empty((*x.shape[:-1], 2 * n), dtype=x.dtype, device=x.device)
+    ts = [x, w, y] + ([x_out] if x_out is not None else [])
+    _check_cuda(*ts)
+    if not all(t.is_contiguous() for t in ts):
+        raise ValueError("swiglu_fc1_fwd needs contiguous tensors")
+    with torch.cuda.device(x.device):
+        st = lib.swiglu_fc1_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                x_out.data_ptr() if x_out is not None else None, M, n, K,
+                                _DTYPE[x.dtype], _stream_handle(x, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_fc1_fwd")
+    return (y, x_out) if x_out is not None else y
+
+
+def fc1_timeout_flag() -> int:
+    out = ctypes.c_int(0)
+    st = lib.swiglu_fc1_timeout_flag(ctypes.byref(out))
+    if st != 0:
+        raise SwigluError(st, "swiglu_fc1_timeout_flag")
+    return int(out.value)
+
+
+__all__ = ["swiglu_fc1_fwd", "fc1_timeout_flag", "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd", "bias_bwd_workspace_bytes",
            "swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd", "status_string", "SwigluError", "lib",
            "SWIGLU_F32", "SWIGLU_BF16", "EXPORTS", "LIB_PATH"]

@@ -5,8 +5,9 @@
 Run it as a script (or load it by path): importing the package itself needs
 the built library.
 
-The library is one translation unit (the C ABI plus the kernel templates it
-instantiates), linked against the static CUDA runtime so the .so depends on
+The library is two translation units (the C ABI with the streaming kernel
+templates it instantiates, and the tensor-core linear_fc1 + SwiGLU kernel),
+compiled in parallel and linked against the static CUDA runtime so the .so depends on
 nothing but the driver.  No fast-math: the kernels choose every approximate
 operation explicitly and must keep subnormal results.
 """
@@ -22,7 +23,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libswiglu.so")
-SOURCES = [os.path.join(CSRC, "swiglu_abi.cu")]
+SOURCES = [os.path.join(CSRC, "swiglu_abi.cu"), os.path.join(CSRC, "fc1_swiglu.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,12 +34,21 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: libswiglu needs the CUDA toolkit to build")
 
 
-def command(out: str = LIB, ptxas_info: bool = False):
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-           "-shared", "-cudart", "static", "-I", INCLUDE, "-I", CSRC, "-o", out, *SOURCES]
-    if ptxas_info:
-        cmd.insert(1, "-Xptxas=-v")
-    return cmd
+COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2"]
+
+
+def compile_commands(out: str = LIB, ptxas_info: bool = False):
+    """One nvcc -c per translation unit (run in parallel), then one link."""
+    objs, cmds = [], []
+    for src in SOURCES:
+        obj = out + "." + os.path.splitext(os.path.basename(src))[0] + ".o"
+        cmd = [nvcc(), *ARCH, *COMMON, "-I", INCLUDE, "-I", CSRC, "-c", "-o", obj, src]
+        if ptxas_info:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        cmds.append(cmd)
+    link = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", out, *objs]
+    return cmds, link, objs
 
 
 def _stale(out: str) -> bool:
@@ -53,8 +63,18 @@ def _stale(out: str) -> bool:
 def build(force: bool = False, ptxas_info: bool = False, out: str = LIB) -> str:
     if force or ptxas_info or _stale(out):
         tmp = out + ".tmp%d" % os.getpid()
-        subprocess.run(command(tmp, ptxas_info), check=True)
-        os.replace(tmp, out)
+        cmds, link, objs = compile_commands(tmp, ptxas_info)
+        procs = [subprocess.Popen(c) for c in cmds]
+        codes = [p.wait() for p in procs]
+        try:
+            if any(codes):
+                raise subprocess.CalledProcessError(max(codes), cmds[codes.index(max(codes))])
+            subprocess.run(link, check=True)
+            os.replace(tmp, out)
+        finally:
+            for o in objs:
+                if os.path.exists(o):
+                    os.remove(o)
     return out
 
 

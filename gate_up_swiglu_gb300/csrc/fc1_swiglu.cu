@@ -1,0 +1,411 @@
+// fc1_swiglu.cu -- linear_fc1 with the SwiGLU activation fused into its
+// epilogue, on the sm_100-class tensor cores (tcgen05, TMEM, TMA).
+//
+// Megatron's MLP computes fc1 = X W^T (W: [2n, K], rows [0, n) the gate
+// projection, [n, 2n) the up projection) and then silu(fc1[:, :n]) *
+// fc1[:, n:] (Liger-Kernel Megatron SwiGLU page, §Background).  Here each CTA
+// owns a 128-row x 128-column tile of y: its tensor-core accumulator is
+// 128 x 256 fp32 in tensor memory, columns [0, 128) the gate dot products for
+// output columns j0 .. j0 + 127 and columns [128, 256) the matching up dot
+// products (W rows n + j0 .. n + j0 + 127), so the epilogue forms y from the
+// fp32 accumulators directly and [M, 2n] never has to pass through HBM unless
+// the caller asks for it (x_out, the buffer a training step saves).
+//
+// Roles (192 threads): warp 0 lane 0 issues the TMA loads of the K slabs
+// (64 bf16 = 128 bytes wide, 128-byte swizzle) into a 4-stage shared-memory
+// ring; warp 1 allocates 256 TMEM columns and its lane 0 issues
+// tcgen05.mma (M = 128, N = 256, K = 16, bf16 in, fp32 accumulate) and commits
+// each stage back to the producer; warps 2-5 wait for the final commit, read the
+// accumulator with tcgen05.ld (each warp its own 32-lane quarter) and store y.
+//
+// Every wait on an mbarrier gives up after kTimeoutNs of %globaltimer time,
+// raises the sticky flag g_fc1_timeout and lets the CTA drain and free its
+// tensor memory, so a fault in the pipeline cannot hang the GPU.
+#include <cuda.h>  // CUtensorMap and its encoding enums (the encoder is fetched at run time)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "abi_internal.h"
+#include "swiglu.h"
+#include "swiglu_kernels.cuh"
+
+namespace fc1 {
+
+constexpr int BM = 128;           // rows of X per tile (MMA M)
+constexpr int BN = 128;           // output columns per tile
+constexpr int UMMA_N = 2 * BN;    // accumulator columns: gate then up
+constexpr int BK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int UMMA_K = 16;        // K per tcgen05.mma of kind::f16
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
+constexpr int B_BYTES = UMMA_N * BK * 2;      // 32 KiB (gate rows, then up rows)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 256;
+constexpr int kThreads = 192;
+constexpr int kBarrierBytes = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kBarrierBytes + 1024;  // + alignment slack
+constexpr unsigned long long kTimeoutNs = 2000000000ull;                  // 2 s
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 =
+// 0), N / 8 in bits 17-22, M / 16 in bits 24-28.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(UMMA_N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ int g_fc1_timeout = 0;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity; false (and the timeout
+// flag raised) if it does not complete within kTimeoutNs.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (now_ns() - t0 > kTimeoutNs) {
+            atomicExch(&g_fc1_timeout, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand laid out by TMA with
+// the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart
+// (stride byte offset), descriptor version 1 (bits 46-47), swizzle mode 2
+// (128 bytes, bits 61-63).  The leading byte offset is unused in this mode.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(kInstrDesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes (one
+// lane = one row per thread).
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fc1_swiglu_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                      __nv_bfloat16 *__restrict__ y, __nv_bfloat16 *__restrict__ x_out, int M, int n,
+                      int K) {
+    extern __shared__ unsigned char smem_raw[];
+    // TMA destinations with the 128-byte swizzle must sit on 1024-byte boundaries
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sa = smem_addr(smem);
+    const uint32_t sb = sa + STAGES * A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
+    const uint32_t tmem_full = smem_addr(bars + 2 * STAGES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM;  // M varies fastest: co-resident CTAs share W tiles in L2
+    const int j0 = blockIdx.y * BN;
+    const int kblocks = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(tmem_full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer: TMA loads of the K slabs
+        int issued = 0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1;
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1)) break;
+            const uint32_t full = full0 + 8 * s;
+            mbar_arrive_expect_tx(full, STAGE_BYTES);
+            tma_load_2d(sa + s * A_BYTES, &tm_x, full, kb * BK, m0);
+            tma_load_2d(sb + s * B_BYTES, &tm_w, full, kb * BK, j0);
+            tma_load_2d(sb + s * B_BYTES + B_BYTES / 2, &tm_w, full, kb * BK, n + j0);
+            issued = kb + 1;
+        }
+        // every stage's last load has landed before the CTA may end
+        for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
+            mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1;
+            if (!mbar_wait(full0 + 8 * s, ph)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                const uint64_t a = smem_desc_sw128(sa + s * A_BYTES + kk * UMMA_K * 2);
+                const uint64_t b = smem_desc_sw128(sb + s * B_BYTES + kk * UMMA_K * 2);
+                mma_bf16(tmem, a, b, (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs are done
+        }
+        mma_commit(tmem_full);  // the accumulator is final once all MMAs are done
+    } else if (warp >= 2) {
+        // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+        const int quarter = warp & 3;
+        const int row = m0 + 32 * quarter + lane;
+        const bool ok = mbar_wait(tmem_full, 0);
+        tc_fence_after();
+        if (ok) {
+            const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t gv[32], uv[32];
+                tmem_load32(tbase + c, gv);
+                tmem_load32(tbase + BN + c, uv);
+                tmem_wait_ld();
+                if (row < M) {
+                    uint32_t out[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float r2[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float g = __uint_as_float(gv[i + h]);
+                            const float u = __uint_as_float(uv[i + h]);
+                            const swiglu::Act act = swiglu::activation<swiglu::BF16, false>(g);
+                            r2[h] = __fmul_rn(__fmul_rn(act.silu, u), act.scale);
+                        }
+                        swiglu::BF16::put2(out, i, r2[0], r2[1]);
+                    }
+                    __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                    if (x_out != nullptr) {
+                        uint32_t pg[16], pu[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            swiglu::BF16::put2(pg, i, __uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
+                            swiglu::BF16::put2(pu, i, __uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
+                        }
+                        __nv_bfloat16 *xg = x_out + (int64_t)row * 2 * n + j0 + c;
+                        __nv_bfloat16 *xu = xg + n;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+                            store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::atomic<EncodeTiled> g_encode{nullptr};
+
+swiglu_status_t fail(cudaError_t e) {
+    swiglu_abi::record_cuda_error((int)e);
+    return SWIGLU_ERR_CUDA;
+}
+
+cudaError_t encoder(EncodeTiled &fn) {
+    fn = g_encode.load();
+    if (fn != nullptr) return cudaSuccess;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || p == nullptr) return cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiled>(p);
+    g_encode.store(fn);
+    return cudaSuccess;
+}
+
+// [rows, K] bf16, row-major: a box of 64 K-elements (128 bytes) by 128 rows,
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map(EncodeTiled enc, CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace fc1
+
+extern "C" {
+
+swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x_out, int64_t M,
+                               int64_t n, int64_t K, swiglu_dtype_t dtype, swiglu_stream_t stream) {
+    using namespace fc1;
+    if (dtype != SWIGLU_BF16) return SWIGLU_ERR_DTYPE;
+    if (M < 0 || n < 0 || K < 0) return SWIGLU_ERR_SHAPE;
+    if (M == 0 || n == 0) return SWIGLU_OK;
+    if (K == 0 || n % BN != 0 || K % 8 != 0 || M > INT32_MAX || K > INT32_MAX ||
+        2 * n > INT32_MAX || n / BN > 65535)
+        return SWIGLU_ERR_SHAPE;
+    if (x_in == nullptr || w == nullptr || y == nullptr) return SWIGLU_ERR_NULL;
+    if (((uintptr_t)x_in | (uintptr_t)w | (uintptr_t)y | (uintptr_t)x_out) % 16 != 0)
+        return SWIGLU_ERR_STRIDE;
+    const size_t bx = (size_t)M * K * 2, bw = (size_t)2 * n * K * 2, by = (size_t)M * n * 2,
+                 bo = (size_t)M * 2 * n * 2;
+    if (overlap(y, by, x_in, bx) || overlap(y, by, w, bw)) return SWIGLU_ERR_ALIAS;
+    if (x_out != nullptr && (overlap(x_out, bo, x_in, bx) || overlap(x_out, bo, w, bw) ||
+                             overlap(x_out, bo, y, by)))
+        return SWIGLU_ERR_ALIAS;
+
+    EncodeTiled enc;
+    cudaError_t e = encoder(enc);
+    if (e != cudaSuccess) return fail(e);
+    CUtensorMap tm_x, tm_w;
+    if (!make_map(enc, &tm_x, x_in, M, K) || !make_map(enc, &tm_w, w, 2 * n, K))
+        return fail(cudaErrorInvalidValue);
+    static std::atomic<bool> attr_set{false};
+    if (!attr_set.load()) {
+        e = cudaFuncSetAttribute(fc1_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
+        if (e != cudaSuccess) return fail(e);
+        attr_set.store(true);
+    }
+    const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)(n / BN));
+    fc1_swiglu_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
+        tm_x, tm_w, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
+        (int)n, (int)K);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SWIGLU_OK : fail(e);
+}
+
+swiglu_status_t swiglu_fc1_timeout_flag(int *flag) {
+    if (flag == nullptr) return SWIGLU_ERR_NULL;
+    cudaError_t e = cudaMemcpyFromSymbol(flag, fc1::g_fc1_timeout, sizeof(int));
+    return e == cudaSuccess ? SWIGLU_OK : fc1::fail(e);
+}
+
+}  // extern "C"

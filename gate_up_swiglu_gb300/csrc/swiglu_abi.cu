@@ -10,6 +10,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "abi_internal.h"
 #include "swiglu.h"
 #include "swiglu_kernels.cuh"
 
@@ -22,6 +23,12 @@ swiglu_status_t cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return SWIGLU_ERR_CUDA;
 }
+
+}  // namespace
+
+void swiglu_abi::record_cuda_error(int err) { g_last_cuda_error = err; }
+
+namespace {
 
 int elem_bytes(swiglu_dtype_t dt) {
     switch (dt) {

@@ -212,6 +212,36 @@ swiglu_status_t swiglu_gateup_bias_bwd_noalloc(const void *dy, const void *x, co
                                                int64_t dx_row_stride, swiglu_dtype_t dtype,
                                                int in_place, swiglu_stream_t stream);
 
+/*
+ * linear_fc1 with the activation fused into its epilogue (tensor cores).
+ * Megatron's MLP produces the [tokens, 2n] buffer as fc1 = X W^T
+ * (Liger-Kernel Megatron SwiGLU page, §Background: linear_fc1 is one
+ * ColumnParallelLinear whose output holds gate and up side by side); this call
+ * computes
+ *   y[m, j] = silu(fc1[m, j]) * fc1[m, n + j],   fc1 = X W^T (fp32 accumulate)
+ * directly from the fp32 accumulators, without writing fc1 to memory unless
+ * x_out is given (then fc1, rounded to bf16, is stored there too, as a training
+ * step saves it for swiglu_gateup_bwd).  bias-free, bf16 only.
+ *   X     [M, K]  bf16, row-major, contiguous         (read)
+ *   W     [2n, K] bf16, row-major (nn.Linear weight: rows [0, n) gate,
+ *                 rows [n, 2n) up), contiguous         (read)
+ *   y     [M, n]  bf16, contiguous                     (written)
+ *   x_out [M, 2n] bf16, contiguous, or NULL            (written)
+ * Requirements: n a multiple of 128 and at most 128 * 65535, K a multiple of 8,
+ * M, K, 2n below 2^31 (else SWIGLU_ERR_SHAPE); all pointers 16-byte aligned
+ * (else SWIGLU_ERR_STRIDE); outputs overlap no input and each other
+ * (SWIGLU_ERR_ALIAS); dtype SWIGLU_BF16 (else SWIGLU_ERR_DTYPE).  M == 0 or
+ * n == 0 is an empty call.  Each CTA bounds its internal waits; a wait that
+ * times out raises the flag read by swiglu_fc1_timeout_flag (results of that
+ * call are then undefined).
+ */
+swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x_out, int64_t M,
+                               int64_t n, int64_t K, swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+/* *flag = 1 if any swiglu_fc1_fwd launch so far gave up on an internal wait,
+ * else 0.  Synchronises with the current device. */
+swiglu_status_t swiglu_fc1_timeout_flag(int *flag);
+
 /* Static English text for a status code; never NULL. */
 const char *swiglu_status_string(swiglu_status_t status);
 

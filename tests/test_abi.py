@@ -35,7 +35,8 @@ def test_header_declares_expected_calls():
         ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
          "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
          "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-         "swiglu_gateup_bias_bwd_noalloc", "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
+         "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
+         "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
 
 
 def test_library_exports_every_declared_symbol(sw):
@@ -193,6 +194,28 @@ def test_bias_rejections(sw):
     assert b(ws=BIAS) == -5              # workspace over bias
     assert b(bias=DX) == -5              # bias under the written dx
     assert b(ws=WS + 4) == -7            # misaligned workspace
+
+
+def test_fc1_rejections(sw):
+    f = lambda **k: sw.lib.swiglu_fc1_fwd(  # noqa: E731
+        k.get("x", X), k.get("w", W), k.get("y", Y), k.get("xo", None), k.get("M", 256),
+        k.get("n", 256), k.get("K", 512), k.get("dt", BF16), None)
+    assert f(dt=F32) == -2
+    assert f(M=-1) == -3
+    assert f(M=0, x=None) == 0
+    assert f(n=100) == -3          # n must be a multiple of 128
+    assert f(K=70) == -3           # K must be a multiple of 8
+    assert f(K=0) == -3
+    assert f(x=None) == -1
+    assert f(w=None) == -1
+    assert f(y=None) == -1
+    assert f(x=X + 8) == -4        # 16-byte alignment
+    assert f(xo=DX + 2) == -4
+    assert f(y=X + 4096) == -5     # y inside X
+    assert f(y=W) == -5
+    assert f(xo=Y + 64) == -5      # x_out over y
+    assert f(xo=X) == -5
+    assert sw.lib.swiglu_fc1_timeout_flag(None) == -1
 
 
 def test_import_fails_loudly_without_the_library(tmp_path):
