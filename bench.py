@@ -446,7 +446,10 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
                 "bwd_frac_of_measured": round(gbs(w.bwd_bytes(), b_ms) / peak, 4),
                 "note": extra_note, "reps": reps}
 
+    fc1 = measure_fc1(sw, dev, stream, reps=max(5, min(reps, 20)))
+
     return {
+        "fc1_swiglu_tcgen05": fc1,
         "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "
                                           "(one CTA per row); GB/s on the plain algorithmic bytes"),
         "bias": row(bf, bb, f"[2n] bias; bwd includes the column-sum pass over a "
@@ -462,6 +465,42 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
             "what": "GateUpSwiGLU forward + torch.autograd.grad, 3D input, out of place",
             "reps": reps, "ms": round(ag_ms, 4)},
     }
+
+
+def measure_fc1(sw, dev, stream, reps):
+    """linear_fc1 + SwiGLU of a Llama-3-8B MLP (X [8192, 4096], W [28672, 4096],
+    bf16) on the tensor cores, against cuBLAS (torch.matmul) followed by the
+    separate activation kernel."""
+    M, K, n = 8192, 4096, 14336
+    g = torch.Generator(device=dev).manual_seed(3)
+    X = torch.randn(M, K, generator=g, device=dev).to(torch.bfloat16)
+    Wt = (torch.randn(2 * n, K, generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+    y = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+    fc1 = torch.empty(M, 2 * n, dtype=torch.bfloat16, device=dev)
+    flops = 2.0 * M * K * 2 * n
+    fused = _event_ms(lambda: sw.swiglu_fc1_fwd(X, Wt, y, stream=stream), stream, reps)
+    fused_fc1 = _event_ms(lambda: sw.swiglu_fc1_fwd(X, Wt, y, fc1, stream=stream), stream, reps)
+
+    def two_step():
+        torch.matmul(X, Wt.T, out=fc1)
+        sw.swiglu_gateup_fwd(fc1, y, stream=stream)
+
+    cublas = _event_ms(two_step, stream, reps)
+    gemm_only = _event_ms(lambda: torch.matmul(X, Wt.T, out=fc1), stream, reps)
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        peak = 1900.0
+    tf = lambda ms: flops / (ms * 1e-3) / 1e12  # noqa: E731
+    return {"shape": "X [8192, 4096] x W [28672, 4096] bf16 -> y [8192, 14336]", "reps": reps,
+            "fused_ms": round(fused, 4), "fused_tflops": round(tf(fused), 1),
+            "fused_frac_of_measured_bf16": round(tf(fused) / peak, 4),
+            "fused_with_fc1_out_ms": round(fused_fc1, 4),
+            "cublas_gemm_plus_swiglu_ms": round(cublas, 4),
+            "cublas_gemm_only_ms": round(gemm_only, 4),
+            "cublas_gemm_tflops": round(tf(gemm_only), 1), "peak_bf16_tflops": peak}
 
 
 def l2_note(w: W.Workload) -> str:

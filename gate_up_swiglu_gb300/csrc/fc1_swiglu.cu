@@ -11,12 +11,14 @@
 // fp32 accumulators directly and [M, 2n] never has to pass through HBM unless
 // the caller asks for it (x_out, the buffer a training step saves).
 //
-// Roles (192 threads): warp 0 lane 0 issues the TMA loads of the K slabs
-// (64 bf16 = 128 bytes wide, 128-byte swizzle) into a 4-stage shared-memory
-// ring; warp 1 allocates 256 TMEM columns and its lane 0 issues
-// tcgen05.mma (M = 128, N = 256, K = 16, bf16 in, fp32 accumulate) and commits
-// each stage back to the producer; warps 2-5 wait for the final commit, read the
-// accumulator with tcgen05.ld (each warp its own 32-lane quarter) and store y.
+// Persistent CTAs, one per SM.  Roles (192 threads): warp 0 lane 0 issues the
+// TMA loads of the K slabs (64 bf16 = 128 bytes wide, 128-byte swizzle) into a
+// 4-stage shared-memory ring; warp 1 allocates all 512 TMEM columns (two
+// accumulators) and its lane 0 issues tcgen05.mma (M = 128, N = 256, K = 16,
+// bf16 in, fp32 accumulate) and commits each stage back to the producer and
+// each finished accumulator to the epilogue; warps 2-5 read an accumulator
+// with tcgen05.ld (each warp its own 32-lane quarter), hand it back, and store
+// y while the tensor cores fill the other one.
 //
 // Every wait on an mbarrier gives up after kTimeoutNs of %globaltimer time,
 // raises the sticky flag g_fc1_timeout and lets the CTA drain and free its
@@ -43,7 +45,7 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KiB
 constexpr int B_BYTES = UMMA_N * BK * 2;      // 32 KiB (gate rows, then up rows)
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 256;
+constexpr int TMEM_COLS = 2 * UMMA_N;  // two accumulators
 constexpr int kThreads = 192;
 constexpr int kBarrierBytes = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kBarrierBytes + 1024;  // + alignment slack
@@ -177,6 +179,15 @@ __device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ...; tile t covers rows
+// (t % tiles_m) * 128 and output columns (t / tiles_m) * 128 (M varies fastest,
+// so co-resident CTAs share W tiles in L2).  Two accumulators in tensor memory
+// (columns [0, 256) and [256, 512)) let the epilogue of one tile run while the
+// tensor cores work on the next.
 __global__ void __launch_bounds__(kThreads, 1)
     fc1_swiglu_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                       __nv_bfloat16 *__restrict__ y, __nv_bfloat16 *__restrict__ x_out, int M, int n,
@@ -188,21 +199,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sa = smem_addr(smem);
     const uint32_t sb = sa + STAGES * A_BYTES;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
-    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + STAGES);
-    const uint32_t tmem_full = smem_addr(bars + 2 * STAGES);
+    // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done
+    const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * STAGES;
+    const uint32_t acc_full0 = empty0 + 8 * STAGES, acc_empty0 = acc_full0 + 16;
+    const uint32_t mma_done = acc_empty0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM;  // M varies fastest: co-resident CTAs share W tiles in L2
-    const int j0 = blockIdx.y * BN;
     const int kblocks = (K + BK - 1) / BK;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles = tiles_m * (n / BN);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(tmem_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);  // one tcgen05.commit
+            mbar_init(acc_empty0 + 8 * a, 4); // one arrival per epilogue warp
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
@@ -220,52 +239,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---- producer: TMA loads of the K slabs
-        int issued = 0;
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (kb / STAGES) & 1;
-            if (!mbar_wait(empty0 + 8 * s, ph ^ 1)) break;
-            const uint32_t full = full0 + 8 * s;
-            mbar_arrive_expect_tx(full, STAGE_BYTES);
-            tma_load_2d(sa + s * A_BYTES, &tm_x, full, kb * BK, m0);
-            tma_load_2d(sb + s * B_BYTES, &tm_w, full, kb * BK, j0);
-            tma_load_2d(sb + s * B_BYTES + B_BYTES / 2, &tm_w, full, kb * BK, n + j0);
-            issued = kb + 1;
+        // ---- producer: TMA loads of the K slabs, one ring across all tiles
+        int it = 0;
+        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+            const int m0 = (t % tiles_m) * BM, j0 = (t / tiles_m) * BN;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t full = full0 + 8 * s;
+                mbar_arrive_expect_tx(full, STAGE_BYTES);
+                tma_load_2d(sa + s * A_BYTES, &tm_x, full, kb * BK, m0);
+                tma_load_2d(sb + s * B_BYTES, &tm_w, full, kb * BK, j0);
+                tma_load_2d(sb + s * B_BYTES + B_BYTES / 2, &tm_w, full, kb * BK, n + j0);
+            }
         }
         // every stage's last load has landed before the CTA may end
-        for (int kb = issued > STAGES ? issued - STAGES : 0; kb < issued; ++kb)
-            mbar_wait(full0 + 8 * (kb % STAGES), (kb / STAGES) & 1);
+        for (int k = it > STAGES ? it - STAGES : 0; k < it; ++k)
+            mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t ph = (kb / STAGES) & 1;
-            if (!mbar_wait(full0 + 8 * s, ph)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                const uint64_t a = smem_desc_sw128(sa + s * A_BYTES + kk * UMMA_K * 2);
-                const uint64_t b = smem_desc_sw128(sb + s * B_BYTES + kk * UMMA_K * 2);
-                mma_bf16(tmem, a, b, (kb | kk) != 0 ? 1u : 0u);
+        int it = 0, lt = 0;
+        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            if (!mbar_wait(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1)) {
+                *abort_flag = 1;
+                break;
             }
-            mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs are done
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(full0 + 8 * s, (it / STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                    const uint64_t a = smem_desc_sw128(sa + s * A_BYTES + kk * UMMA_K * 2);
+                    const uint64_t b = smem_desc_sw128(sb + s * B_BYTES + kk * UMMA_K * 2);
+                    mma_bf16(d, a, b, (kb | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs are done
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            mma_commit(acc_full0 + 8 * acc);  // this accumulator is final
         }
-        mma_commit(tmem_full);  // the accumulator is final once all MMAs are done
+        // all issued MMAs have finished before tensor memory is released
+        mma_commit(mma_done);
+        mbar_wait(mma_done, 0);
     } else if (warp >= 2) {
         // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
         const int quarter = warp & 3;
-        const int row = m0 + 32 * quarter + lane;
-        const bool ok = mbar_wait(tmem_full, 0);
-        tc_fence_after();
-        if (ok) {
-            const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16);
+        int lt = 0;
+        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
+            const int acc = lt & 1;
+            const int m0 = (t % tiles_m) * BM, j0 = (t / tiles_m) * BN;
+            const int row = m0 + 32 * quarter + lane;
+            if (!mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(acc * UMMA_N);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t gv[32], uv[32];
                 tmem_load32(tbase + c, gv);
                 tmem_load32(tbase + BN + c, uv);
                 tmem_wait_ld();
+                if (c + 32 == BN) {
+                    // the whole accumulator has been read: hand it back to the MMA issuer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
+                }
                 if (row < M) {
                     uint32_t out[16];
 #pragma unroll
@@ -394,7 +449,13 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
         if (e != cudaSuccess) return fail(e);
         attr_set.store(true);
     }
-    const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)(n / BN));
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(e);
+    const int64_t tiles = ((M + BM - 1) / BM) * (n / BN);
+    if (tiles > INT32_MAX) return SWIGLU_ERR_SHAPE;
+    const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
     fc1_swiglu_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
         tm_x, tm_w, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
         (int)n, (int)K);
