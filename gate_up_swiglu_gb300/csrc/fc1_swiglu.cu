@@ -173,19 +173,36 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// outputs are written once and not reread here: evict-first, so they do not
+// push the reused X and W tiles out of L2
 __device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+// Tile order: groups of kGroupM row tiles; within a group the row tile varies
+// fastest.  A wave of co-resident CTAs then covers about kGroupM row tiles x
+// (SMs / kGroupM) column tiles, so its X rows stay in L2 across the whole group
+// and each W tile is fetched from HBM once per group instead of once per wave.
+constexpr int kGroupM = 16;
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &j0) {
+    const int per_group = kGroupM * tiles_n;
+    const int g = t / per_group;
+    const int first = g * kGroupM;
+    const int gm = min(kGroupM, tiles_m - first);
+    const int local = t - g * per_group;
+    m0 = (first + local % gm) * BM;
+    j0 = (local / gm) * BN;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Persistent: CTA b takes tiles b, b + gridDim.x, ...; tile t covers rows
-// (t % tiles_m) * 128 and output columns (t / tiles_m) * 128 (M varies fastest,
-// so co-resident CTAs share W tiles in L2).  Two accumulators in tensor memory
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... in the grouped order of
+// tile_coords.  Two accumulators in tensor memory
 // (columns [0, 256) and [256, 512)) let the epilogue of one tile run while the
 // tensor cores work on the next.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -209,7 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = (K + BK - 1) / BK;
     const int tiles_m = (M + BM - 1) / BM;
-    const int tiles = tiles_m * (n / BN);
+    const int tiles_n = n / BN;
+    const int tiles = tiles_m * tiles_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -242,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- producer: TMA loads of the K slabs, one ring across all tiles
         int it = 0;
         for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-            const int m0 = (t % tiles_m) * BM, j0 = (t / tiles_m) * BN;
+            int m0, j0;
+            tile_coords(t, tiles_m, tiles_n, m0, j0);
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int s = it % STAGES;
                 if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1)) {
@@ -301,7 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int lt = 0;
         for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
             const int acc = lt & 1;
-            const int m0 = (t % tiles_m) * BM, j0 = (t / tiles_m) * BN;
+            int m0, j0;
+            tile_coords(t, tiles_m, tiles_n, m0, j0);
             const int row = m0 + 32 * quarter + lane;
             if (!mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1)) {
                 *abort_flag = 1;
