@@ -396,6 +396,283 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------ CTA-pair (2-SM) variant ---
+// The same tile work, but a cluster of two CTAs computes a 256-row tile with
+// tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of X and one half
+// of the W slab (the leader the 128 gate rows, the peer the 128 up rows), the
+// leader's single MMA thread drives both SMs' tensor cores, and each CTA's
+// tensor memory receives the accumulator of its own 128 rows (gate columns
+// [0, 128), up columns [128, 256) as before).  A CTA's stage shrinks to 32 KiB,
+// so six stages fit the 192 KiB ring: the pipeline hides twice the latency of
+// the one-CTA kernel for the same shared memory.
+constexpr int PAIR_M = 2 * BM;
+constexpr int B2_BYTES = BN * BK * 2;                 // this CTA's half of the W slab
+constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;      // 32 KiB
+constexpr int STAGES2 = (192 * 1024) / STAGE2_BYTES;  // 6
+static_assert(2 * STAGES2 + 7 <= 32, "barriers fit their 256-byte region");
+constexpr uint32_t kInstrDesc2 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                 ((uint32_t)(UMMA_N >> 3) << 17) | ((uint32_t)(PAIR_M >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of this CTA's shared variable `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+    return out;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA (the leader's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(kInstrDesc2), "r"(acc)
+        : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs once the pair MMAs issued
+// so far are done.
+__device__ __forceinline__ void mma_commit_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_local_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void pair_tile_coords(int t, int tiles_m2, int tiles_n, int &m0, int &j0) {
+    const int per_group = kGroupM * tiles_n;
+    const int g = t / per_group;
+    const int first = g * kGroupM;
+    const int gm = min(kGroupM, tiles_m2 - first);
+    const int local = t - g * per_group;
+    m0 = (first + local % gm) * PAIR_M;
+    j0 = (local / gm) * BN;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    fc1_swiglu_pair_kernel(const __grid_constant__ CUtensorMap tm_x,
+                           const __grid_constant__ CUtensorMap tm_w, __nv_bfloat16 *__restrict__ y,
+                           __nv_bfloat16 *__restrict__ x_out, int M, int n, int K) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sa = smem_addr(smem);
+    const uint32_t sb = sa + STAGES2 * A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES2 * STAGE2_BYTES);
+    // barriers: full[STAGES2], empty[STAGES2], acc_full[2], acc_empty[2], mma_done
+    const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * STAGES2;
+    const uint32_t acc_full0 = empty0 + 8 * STAGES2, acc_empty0 = acc_full0 + 16;
+    const uint32_t mma_done = acc_empty0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES2 + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kblocks = (K + BK - 1) / BK;
+    const int tiles_m2 = (M + PAIR_M - 1) / PAIR_M;
+    const int tiles_n = n / BN;
+    const int tiles = tiles_m2 * tiles_n;
+    const int cluster_id = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(full0 + 8 * s, 1);   // the leader's producer (plus both CTAs' bytes)
+            mbar_init(empty0 + 8 * s, 1);  // the leader's commit, multicast to both CTAs
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full0 + 8 * a, 1);   // the leader's commit, multicast
+            mbar_init(acc_empty0 + 8 * a, 8);  // the epilogue warps of both CTAs (leader's copy)
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer (both CTAs): this CTA's X rows and its half of the W slab
+        int it = 0;
+        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters) {
+            int m0, j0;
+            pair_tile_coords(t, tiles_m2, tiles_n, m0, j0);
+            const int my_m0 = m0 + BM * (int)rank;
+            const int w_row = leader ? j0 : n + j0;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES2;
+                if (!mbar_wait(empty0 + 8 * s, ((it / STAGES2) & 1) ^ 1)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t full_leader = map_to_rank(full0 + 8 * s, 0);
+                if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE2_BYTES);
+                tma_load_2d_pair(sa + s * A_BYTES, &tm_x, full_leader, kb * BK, my_m0);
+                tma_load_2d_pair(sb + s * B2_BYTES, &tm_w, full_leader, kb * BK, w_row);
+            }
+        }
+        // the leader's full barriers count both CTAs' bytes: once their last
+        // phases complete, every load of the pair has landed
+        if (leader)
+            for (int k = it > STAGES2 ? it - STAGES2 : 0; k < it; ++k)
+                mbar_wait(full0 + 8 * (k % STAGES2), (k / STAGES2) & 1);
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---- MMA issuer (leader only): drives the tensor cores of both SMs
+        int it = 0, lt = 0;
+        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters, ++lt) {
+            const int acc = lt & 1;
+            if (!mbar_wait(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
+            bool ok = true;
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES2;
+                if (!mbar_wait(full0 + 8 * s, (it / STAGES2) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                    const uint64_t a = smem_desc_swizzled(sa + s * A_BYTES + kk * UMMA_K * 2);
+                    const uint64_t b = smem_desc_swizzled(sb + s * B2_BYTES + kk * UMMA_K * 2);
+                    mma_bf16_pair(d, a, b, (kb | kk) != 0 ? 1u : 0u);
+                }
+                mma_commit_both(empty0 + 8 * s);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            mma_commit_both(acc_full0 + 8 * acc);
+        }
+        mma_commit_local_pair(mma_done);
+        mbar_wait(mma_done, 0);
+    } else if (warp >= 2) {
+        // ---- epilogue (both CTAs): this CTA's 128 rows of the accumulator
+        const int quarter = warp & 3;
+        const uint32_t acc_empty_leader0 = map_to_rank(acc_empty0, 0);
+        int lt = 0;
+        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters, ++lt) {
+            const int acc = lt & 1;
+            int m0, j0;
+            pair_tile_coords(t, tiles_m2, tiles_n, m0, j0);
+            const int row = m0 + BM * (int)rank + 32 * quarter + lane;
+            if (!mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(acc * UMMA_N);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t gv[32], uv[32];
+                tmem_load32(tbase + c, gv);
+                tmem_load32(tbase + BN + c, uv);
+                tmem_wait_ld();
+                if (c + 32 == BN) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8 * acc);
+                }
+                if (row < M) {
+                    uint32_t out[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float r2[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const float g = __uint_as_float(gv[i + h]);
+                            const float u = __uint_as_float(uv[i + h]);
+                            const swiglu::Act act = swiglu::activation<swiglu::BF16, false>(g);
+                            r2[h] = __fmul_rn(__fmul_rn(act.silu, u), act.scale);
+                        }
+                        swiglu::BF16::put2(out, i, r2[0], r2[1]);
+                    }
+                    __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                    if (x_out != nullptr) {
+                        uint32_t pg[16], pu[16];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            swiglu::BF16::put2(pg, i, __uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
+                            swiglu::BF16::put2(pu, i, __uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
+                        }
+                        __nv_bfloat16 *xg = x_out + (int64_t)row * 2 * n + j0 + c;
+                        __nv_bfloat16 *xu = xg + n;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+                            store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still signal it
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -473,7 +750,7 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
         return fail(cudaErrorInvalidValue);
     static std::atomic<bool> attr_set{false};
     if (!attr_set.load()) {
-        e = cudaFuncSetAttribute(fc1_swiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fc1_swiglu_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES);
         if (e != cudaSuccess) return fail(e);
         attr_set.store(true);
@@ -482,10 +759,11 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
-    const int64_t tiles = ((M + BM - 1) / BM) * (n / BN);
+    const int64_t tiles = ((M + PAIR_M - 1) / PAIR_M) * (n / BN);  // 256-row pair tiles
     if (tiles > INT32_MAX) return SWIGLU_ERR_SHAPE;
-    const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
-    fc1_swiglu_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
+    const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
+    const dim3 grid((unsigned)(2 * (pairs > 0 ? pairs : 1)));
+    fc1_swiglu_pair_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
         tm_x, tm_w, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
         (int)n, (int)K);
     e = cudaGetLastError();
