@@ -1,27 +1,30 @@
 // fc1_swiglu.cu -- linear_fc1 with the SwiGLU activation fused into its
-// epilogue, on the sm_100-class tensor cores (tcgen05, TMEM, TMA).
+// epilogue, on the sm_100-class tensor cores (tcgen05, TMEM, TMA, CTA pairs).
 //
 // Megatron's MLP computes fc1 = X W^T (W: [2n, K], rows [0, n) the gate
 // projection, [n, 2n) the up projection) and then silu(fc1[:, :n]) *
-// fc1[:, n:] (Liger-Kernel Megatron SwiGLU page, §Background).  Here each CTA
-// owns a 128-row x 128-column tile of y: its tensor-core accumulator is
-// 128 x 256 fp32 in tensor memory, columns [0, 128) the gate dot products for
-// output columns j0 .. j0 + 127 and columns [128, 256) the matching up dot
-// products (W rows n + j0 .. n + j0 + 127), so the epilogue forms y from the
-// fp32 accumulators directly and [M, 2n] never has to pass through HBM unless
-// the caller asks for it (x_out, the buffer a training step saves).
+// fc1[:, n:] (Liger-Kernel Megatron SwiGLU page, §Background).  Here a cluster
+// of two CTAs owns a 256-row x 128-column tile of y.  Its tensor-core
+// accumulator (one 128 x 256 fp32 block per CTA, in tensor memory) holds in
+// columns [0, 128) the gate dot products for output columns j0 .. j0 + 127 and
+// in columns [128, 256) the matching up dot products (W rows n + j0 ..), so the
+// epilogue forms y from the fp32 accumulators directly and [M, 2n] never has
+// to pass through HBM unless the caller asks for it (x_out, the buffer a
+// training step saves).
 //
-// Persistent CTAs, one per SM.  Roles (192 threads): warp 0 lane 0 issues the
-// TMA loads of the K slabs (BK bf16 wide, swizzled) into a 192 KiB
-// shared-memory ring; warp 1 allocates all 512 TMEM columns (two
-// accumulators) and its lane 0 issues tcgen05.mma (M = 128, N = 256, K = 16,
-// bf16 in, fp32 accumulate) and commits each stage back to the producer and
-// each finished accumulator to the epilogue; warps 2-5 read an accumulator
-// with tcgen05.ld (each warp its own 32-lane quarter), hand it back, and store
-// y while the tensor cores fill the other one.
+// Persistent CTA pairs, one CTA per SM.  Roles (192 threads per CTA): warp 0
+// lane 0 of each CTA TMA-loads that CTA's 128 rows of X and its half of the W
+// slab (64 bf16 of K, 128-byte swizzle) into a 6-stage, 192 KiB ring; warp 1
+// of each CTA takes part in allocating all 512 TMEM columns (two
+// accumulators), and lane 0 of the leader's warp 1 issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16, bf16 in, fp32
+// accumulate) for both SMs, multicasting each stage's release and each
+// finished accumulator to both CTAs; warps 2-5 of each CTA read their CTA's
+// accumulator with tcgen05.ld (each warp its own 32-lane quarter), hand it
+// back to the leader and store y while the tensor cores fill the other one.
 //
 // Every wait on an mbarrier gives up after kTimeoutNs of %globaltimer time,
-// raises the sticky flag g_fc1_timeout and lets the CTA drain and free its
+// raises the sticky flag g_fc1_timeout and lets the pair drain and free its
 // tensor memory, so a fault in the pipeline cannot hang the GPU.
 #include <cuda.h>  // CUtensorMap and its encoding enums (the encoder is fetched at run time)
 #include <cuda_bf16.h>
@@ -39,29 +42,18 @@ namespace fc1 {
 constexpr int BM = 128;           // rows of X per tile (MMA M)
 constexpr int BN = 128;           // output columns per tile
 constexpr int UMMA_N = 2 * BN;    // accumulator columns: gate then up
-// K per stage: 64 bf16 = one 128-byte swizzle row, 4 stages of 48 KiB.  (BK
-// = 32 with the 64-byte swizzle and 8 stages of 24 KiB measured 25 % slower on
-// GB300.)
+// K per stage: 64 bf16 = one 128-byte swizzle row.  (BK = 32 with the
+// 64-byte swizzle and twice the stages measured 25 % slower on GB300.)
 constexpr int BK = 64;
 constexpr int SWZ_BYTES = BK * 2;             // bytes per swizzled row
 constexpr int UMMA_K = 16;                    // K per tcgen05.mma of kind::f16
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = UMMA_N * BK * 2;      // gate rows, then up rows
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = (192 * 1024) / STAGE_BYTES;
+constexpr int A_BYTES = BM * BK * 2;          // this CTA's 128 rows of X
 static_assert(SWZ_BYTES == 64 || SWZ_BYTES == 128, "64- or 128-byte swizzle");
-static_assert(2 * STAGES + 7 <= 32, "barriers fit their 256-byte region");
 constexpr int TMEM_COLS = 2 * UMMA_N;  // two accumulators
 constexpr int kThreads = 192;
 constexpr int kBarrierBytes = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + kBarrierBytes + 1024;  // + alignment slack
+constexpr int SMEM_BYTES = 192 * 1024 + kBarrierBytes + 1024;  // ring + barriers + alignment slack
 constexpr unsigned long long kTimeoutNs = 2000000000ull;                  // 2 s
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
-// 4-5 = 1), A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 =
-// 0), N / 8 in bits 17-22, M / 16 in bits 24-28.
-constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                ((uint32_t)(UMMA_N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 __device__ int g_fc1_timeout = 0;
 
@@ -112,15 +104,6 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return true;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major operand laid out by TMA with
 // the SWZ_BYTES swizzle: rows of SWZ_BYTES bytes, 8-row groups 8 * SWZ_BYTES
 // apart (stride byte offset), descriptor version 1 (bits 46-47), layout type
@@ -135,23 +118,6 @@ __device__ __forceinline__ uint64_t smem_desc_swizzled(uint32_t saddr) {
     d |= (uint64_t)1 << 46;
     d |= layout << 61;
     return d;
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(kInstrDesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -190,226 +156,30 @@ __device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_
 }
 
 // Tile order: groups of kGroupM row tiles; within a group the row tile varies
-// fastest.  A wave of co-resident CTAs then covers about kGroupM row tiles x
-// (SMs / kGroupM) column tiles, so its X rows stay in L2 across the whole group
-// and each W tile is fetched from HBM once per group instead of once per wave.
+// fastest.  A wave of co-resident CTA pairs then covers about kGroupM row tiles
+// x (pairs / kGroupM) column tiles, so its X rows stay in L2 across the whole
+// group and each W tile is fetched from HBM once per group instead of once per
+// wave (waves spanning every row tile read 10x the input bytes from HBM).
 constexpr int kGroupM = 16;
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &m0, int &j0) {
-    const int per_group = kGroupM * tiles_n;
-    const int g = t / per_group;
-    const int first = g * kGroupM;
-    const int gm = min(kGroupM, tiles_m - first);
-    const int local = t - g * per_group;
-    m0 = (first + local % gm) * BM;
-    j0 = (local / gm) * BN;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Persistent: CTA b takes tiles b, b + gridDim.x, ... in the grouped order of
-// tile_coords.  Two accumulators in tensor memory
-// (columns [0, 256) and [256, 512)) let the epilogue of one tile run while the
-// tensor cores work on the next.
-__global__ void __launch_bounds__(kThreads, 1)
-    fc1_swiglu_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                      __nv_bfloat16 *__restrict__ y, __nv_bfloat16 *__restrict__ x_out, int M, int n,
-                      int K) {
-    extern __shared__ unsigned char smem_raw[];
-    // TMA destinations with the 128-byte swizzle must sit on 1024-byte boundaries
-    const uint32_t raw = smem_addr(smem_raw);
-    unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    const uint32_t sa = smem_addr(smem);
-    const uint32_t sb = sa + STAGES * A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    // barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done
-    const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * STAGES;
-    const uint32_t acc_full0 = empty0 + 8 * STAGES, acc_empty0 = acc_full0 + 16;
-    const uint32_t mma_done = acc_empty0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kblocks = (K + BK - 1) / BK;
-    const int tiles_m = (M + BM - 1) / BM;
-    const int tiles_n = n / BN;
-    const int tiles = tiles_m * tiles_n;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(acc_full0 + 8 * a, 1);  // one tcgen05.commit
-            mbar_init(acc_empty0 + 8 * a, 4); // one arrival per epilogue warp
-        }
-        mbar_init(mma_done, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0 && lane == 0) {
-        // ---- producer: TMA loads of the K slabs, one ring across all tiles
-        int it = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
-            int m0, j0;
-            tile_coords(t, tiles_m, tiles_n, m0, j0);
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % STAGES;
-                if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                const uint32_t full = full0 + 8 * s;
-                mbar_arrive_expect_tx(full, STAGE_BYTES);
-                tma_load_2d(sa + s * A_BYTES, &tm_x, full, kb * BK, m0);
-                tma_load_2d(sb + s * B_BYTES, &tm_w, full, kb * BK, j0);
-                tma_load_2d(sb + s * B_BYTES + B_BYTES / 2, &tm_w, full, kb * BK, n + j0);
-            }
-        }
-        // every stage's last load has landed before the CTA may end
-        for (int k = it > STAGES ? it - STAGES : 0; k < it; ++k)
-            mbar_wait(full0 + 8 * (k % STAGES), (k / STAGES) & 1);
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        int it = 0, lt = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
-            const int acc = lt & 1;
-            if (!mbar_wait(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(acc * UMMA_N);
-            bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % STAGES;
-                if (!mbar_wait(full0 + 8 * s, (it / STAGES) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                    const uint64_t a = smem_desc_swizzled(sa + s * A_BYTES + kk * UMMA_K * 2);
-                    const uint64_t b = smem_desc_swizzled(sb + s * B_BYTES + kk * UMMA_K * 2);
-                    mma_bf16(d, a, b, (kb | kk) != 0 ? 1u : 0u);
-                }
-                mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs are done
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                break;
-            }
-            mma_commit(acc_full0 + 8 * acc);  // this accumulator is final
-        }
-        // all issued MMAs have finished before tensor memory is released
-        mma_commit(mma_done);
-        mbar_wait(mma_done, 0);
-    } else if (warp >= 2) {
-        // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
-        const int quarter = warp & 3;
-        int lt = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
-            const int acc = lt & 1;
-            int m0, j0;
-            tile_coords(t, tiles_m, tiles_n, m0, j0);
-            const int row = m0 + 32 * quarter + lane;
-            if (!mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1)) {
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(acc * UMMA_N);
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t gv[32], uv[32];
-                tmem_load32(tbase + c, gv);
-                tmem_load32(tbase + BN + c, uv);
-                tmem_wait_ld();
-                if (c + 32 == BN) {
-                    // the whole accumulator has been read: hand it back to the MMA issuer
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);
-                }
-                if (row < M) {
-                    uint32_t out[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float r2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float g = __uint_as_float(gv[i + h]);
-                            const float u = __uint_as_float(uv[i + h]);
-                            const swiglu::Act act = swiglu::activation<swiglu::BF16, false>(g);
-                            r2[h] = __fmul_rn(__fmul_rn(act.silu, u), act.scale);
-                        }
-                        swiglu::BF16::put2(out, i, r2[0], r2[1]);
-                    }
-                    __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-                    if (x_out != nullptr) {
-                        uint32_t pg[16], pu[16];
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            swiglu::BF16::put2(pg, i, __uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
-                            swiglu::BF16::put2(pu, i, __uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
-                        }
-                        __nv_bfloat16 *xg = x_out + (int64_t)row * 2 * n + j0 + c;
-                        __nv_bfloat16 *xu = xg + n;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-                            store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
-                        }
-                    }
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(TMEM_COLS)
-                     : "memory");
-    }
-}
-
-// ------------------------------------------------ CTA-pair (2-SM) variant ---
-// The same tile work, but a cluster of two CTAs computes a 256-row tile with
+// ------------------------------------------------------ the CTA-pair kernel ---
+// A cluster of two CTAs computes a 256-row tile with
 // tcgen05.mma.cta_group::2: each CTA loads its own 128 rows of X and one half
 // of the W slab (the leader the 128 gate rows, the peer the 128 up rows), the
 // leader's single MMA thread drives both SMs' tensor cores, and each CTA's
 // tensor memory receives the accumulator of its own 128 rows (gate columns
-// [0, 128), up columns [128, 256) as before).  A CTA's stage shrinks to 32 KiB,
-// so six stages fit the 192 KiB ring: the pipeline hides twice the latency of
-// the one-CTA kernel for the same shared memory.
+// [0, 128), up columns [128, 256)).  A CTA's stage is 32 KiB, so six stages
+// fit a 192 KiB ring.  With one CTA per 128 x 256 tile the stage was 48 KiB,
+// four stages hid too little latency and the tensor pipe idled a quarter of
+// the time (1.05 ms against 0.99 ms for the Llama-3-8B fc1 shape).
 constexpr int PAIR_M = 2 * BM;
 constexpr int B2_BYTES = BN * BK * 2;                 // this CTA's half of the W slab
 constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;      // 32 KiB
 constexpr int STAGES2 = (192 * 1024) / STAGE2_BYTES;  // 6
 static_assert(2 * STAGES2 + 7 <= 32, "barriers fit their 256-byte region");
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 =
+// 0), N / 8 in bits 17-22, M / 16 in bits 24-28 (M = 256 across the pair).
 constexpr uint32_t kInstrDesc2 = (1u << 4) | (1u << 7) | (1u << 10) |
                                  ((uint32_t)(UMMA_N >> 3) << 17) | ((uint32_t)(PAIR_M >> 4) << 24);
 
