@@ -67,14 +67,17 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources that define the streaming kernels and their launch configuration
+STREAMING_SOURCES = ("swiglu_kernels.cuh", "silu_root_poly.h", "swiglu_abi.cu")
+
+
 def source_digest() -> str:
-    """Digest of the kernel sources, to tell whether stored ncu counters still
-    describe the current kernels."""
+    """Digest of the streaming kernels' sources, to tell whether stored ncu
+    counters still describe the kernels the bench times."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in STREAMING_SOURCES:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
