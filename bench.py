@@ -57,6 +57,48 @@ def dist_env():
     return ws, rank, local
 
 
+class Replicas:
+    """The ranks of a torchrun launch, or the single process of a plain one.
+
+    The op has no exchange step, so ranks are independent replicas of the
+    workload: they meet only to start and stop the clock together and to take
+    the slowest rank's time.  `backend` is "nccl" on GPUs ("gloo" in the CPU
+    tests of this plumbing)."""
+
+    def __init__(self, backend: str = "nccl", device=None):
+        self.world, self.rank, self.local = dist_env()
+        self.device = device if device is not None else torch.device("cpu")
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            kw = {"device_id": self.device} if backend == "nccl" else {}
+            dist.init_process_group(backend=backend, **kw)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        """The largest of every rank's v (every rank gets it)."""
+        if self.dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    @property
+    def reports(self) -> bool:
+        """Rank 0 alone prints the JSON line."""
+        return self.rank == 0
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -235,12 +277,7 @@ def ours_arm(args, w):
         raise SystemExit("bench.py needs a CUDA GPU (libswiglu has no CPU path)")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pg = None
-    if ws > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group(backend="nccl", device_id=dev)
-        pg = dist
+    ranks = Replicas("nccl", dev)
 
     import importlib.util
 
@@ -251,16 +288,7 @@ def ours_arm(args, w):
     builder.build()
     import gate_up_swiglu_gb300 as sw
 
-    def barrier():
-        if pg is not None:
-            pg.barrier()
-
-    def max_over_ranks(v: float) -> float:
-        if pg is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     x, dy = W.make_inputs(w, dev)
     x = x.contiguous()
@@ -342,7 +370,8 @@ def ours_arm(args, w):
                "sample": f"{srows} of {w.rows} rows (fwd + bwd, {secs:.1f} s single thread), "
                          "scaled to the full workload"}
 
-    if rank != 0:
+    if not ranks.reports:
+        ranks.close()
         return
     peak, peak_src = measured_peaks()
     fb, bb = w.fwd_bytes(), w.bwd_bytes()
@@ -379,8 +408,7 @@ def ours_arm(args, w):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    ranks.close()
 
 
 def _event_ms(fn, stream, reps):
