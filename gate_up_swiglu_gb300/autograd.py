@@ -120,3 +120,53 @@ class GateUpSwiGLU(torch.nn.Module):
             raise ValueError(f"GateUpSwiGLU: dtype {intermediate.dtype} is not supported "
                              "(float32 or bfloat16)")
         return GateUpSwiGLUFunction.apply(intermediate, self.in_place)
+
+
+class Fc1SwiGLUFunction(torch.autograd.Function):
+    """linear_fc1 followed by the activation, y = silu((X W^T)[..., :n]) *
+    (X W^T)[..., n:], with the activation in the tensor-core GEMM's epilogue.
+
+    The forward stores the bf16 fc1 output for the backward (the buffer the
+    Megatron layout keeps); the backward runs the fused activation backward on
+    it -- in place when ``in_place`` -- and then the two plain GEMMs
+    dX = d(fc1) W and dW = d(fc1)^T X through cuBLAS."""
+
+    @staticmethod
+    def forward(ctx, x: torch.Tensor, weight: torch.Tensor, in_place: bool = False):
+        from . import swiglu_fc1_fwd
+
+        y, fc1 = swiglu_fc1_fwd(x.contiguous(), weight.contiguous(), return_fc1=True)
+        ctx.save_for_backward(x, weight, fc1)
+        ctx.in_place = bool(in_place)
+        ctx.already_backward = False
+        return y
+
+    @staticmethod
+    def backward(ctx, dy: torch.Tensor):
+        if ctx.in_place:
+            if ctx.already_backward:
+                raise RuntimeError("Fc1SwiGLUFunction: backward already ran with in_place=True")
+            ctx.already_backward = True
+        x, weight, fc1 = ctx.saved_tensors
+        dfc1 = swiglu_gateup_bwd(dy.contiguous(), fc1, in_place=ctx.in_place)
+        k = x.shape[-1]
+        d2 = dfc1.reshape(-1, dfc1.shape[-1])
+        dx = (d2 @ weight).reshape(x.shape) if ctx.needs_input_grad[0] else None
+        dw = d2.t() @ x.reshape(-1, k) if ctx.needs_input_grad[1] else None
+        return dx, dw, None
+
+
+class Fc1SwiGLU(torch.nn.Module):
+    """Megatron's linear_fc1 (bias-free, gate rows then up rows in one
+    [2 * ffn_hidden, in_features] weight) fused with the activation."""
+
+    def __init__(self, in_features: int, ffn_hidden: int, in_place: bool = False,
+                 device=None, dtype=torch.bfloat16):
+        super().__init__()
+        self.weight = torch.nn.Parameter(
+            torch.empty(2 * ffn_hidden, in_features, device=device, dtype=dtype))
+        torch.nn.init.normal_(self.weight, std=in_features ** -0.5)
+        self.in_place = in_place
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return Fc1SwiGLUFunction.apply(x, self.weight, self.in_place)

@@ -102,3 +102,28 @@ def test_fc1_llama_shape_sampled(sw):
     assert sw.fc1_timeout_flag() == 0
     rows = torch.tensor([0, 1, 127, 128, 4095, 8190, 8191])
     _check(y, fc1, X.cpu(), Wt.cpu(), rows, "fc1 llama")
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_fc1_module_gradients(sw, in_place):
+    """Autograd through the fused fc1 module against float64 torch autograd of
+    the same math (bf16 GEMMs: relative Frobenius error below 1 %)."""
+    from gate_up_swiglu_gb300.autograd import Fc1SwiGLU
+
+    torch.manual_seed(0)
+    M, K, n = 384, 512, 256
+    mod = Fc1SwiGLU(K, n, in_place=in_place, device="cuda")
+    x = torch.randn(3, M // 3, K, device="cuda").to(torch.bfloat16).requires_grad_(True)
+    dy = torch.randn(3, M // 3, n, device="cuda").to(torch.bfloat16)
+    y = mod(x)
+    y.backward(dy)
+    x64 = x.detach().double().requires_grad_(True)
+    w64 = mod.weight.detach().double().requires_grad_(True)
+    f = x64 @ w64.T
+    y64 = F.silu(f[..., :n]) * f[..., n:]
+    y64.backward(dy.double())
+    rel = lambda a, b: float((a.double() - b).norm() / b.norm())  # noqa: E731
+    assert rel(y.detach(), y64.detach()) < 1e-2
+    assert rel(x.grad, x64.grad) < 1e-2
+    assert rel(mod.weight.grad, w64.grad) < 1e-2
+    assert sw.fc1_timeout_flag() == 0
