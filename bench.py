@@ -478,8 +478,10 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
                 "note": extra_note, "reps": reps}
 
     fc1 = measure_fc1(sw, dev, stream, reps=max(5, min(reps, 20)))
+    per_workload = measure_workloads(sw, dev, stream, skip=w.name, reps=max(5, min(reps, 50)))
 
     return {
+        "other_workloads": per_workload,
         "fc1_swiglu_tcgen05": fc1,
         "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "
                                           "(one CTA per row); GB/s on the plain algorithmic bytes"),
@@ -496,6 +498,40 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
             "what": "GateUpSwiGLU forward + torch.autograd.grad, 3D input, out of place",
             "reps": reps, "ms": round(ag_ms, 4)},
     }
+
+
+def measure_workloads(sw, dev, stream, skip, reps):
+    """Forward, backward and in-place backward on every other workload (the
+    tiny fp32 one, the Megatron-shape and Llama-like bf16 ones, the odd-width
+    fp32 one), CUDA events per launch, inputs resident in HBM."""
+    peak, _ = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for name, wl in W.WORKLOADS.items():
+        if name == skip:
+            continue
+        x, dy = W.make_inputs(wl, dev)
+        x = x.contiguous()
+        y = torch.empty((wl.rows, wl.n), dtype=x.dtype, device=dev)
+        dx = torch.empty_like(x)
+        xi = x.clone()
+        f = _event_ms(lambda: sw.swiglu_gateup_fwd(x, y, stream=stream), stream, reps)
+        b = _event_ms(lambda: sw.swiglu_gateup_bwd(dy, x, dx, stream=stream), stream, reps)
+        # the in-place timing overwrites xi each launch; values change, the
+        # work and the arithmetic path do not
+        bi = _event_ms(lambda: sw.swiglu_gateup_bwd(dy, xi, in_place=True, stream=stream),
+                       stream, reps)
+        gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+        out[name] = {
+            "shape": list(wl.shape), "dtype": wl.dtype, "fwd_ms": round(f, 4), "bwd_ms": round(b, 4),
+            "bwd_in_place_ms": round(bi, 4), "fwd_gbs": round(gb(wl.fwd_bytes(), f), 1),
+            "bwd_gbs": round(gb(wl.bwd_bytes(), b), 1),
+            "fwd_frac_of_measured": round(gb(wl.fwd_bytes(), f) / peak, 4),
+            "bwd_frac_of_measured": round(gb(wl.bwd_bytes(), b) / peak, 4),
+            "l2": "inputs exceed L2" if 3 * wl.n * wl.rows * wl.elem_bytes > l2
+                  else "inputs fit in L2 (back-to-back launches: L2-resident)"}
+        del x, dy, y, dx, xi
+    return out
 
 
 def measure_fc1(sw, dev, stream, reps):
