@@ -127,3 +127,21 @@ def test_fc1_module_gradients(sw, in_place):
     assert rel(x.grad, x64.grad) < 1e-2
     assert rel(mod.weight.grad, w64.grad) < 1e-2
     assert sw.fc1_timeout_flag() == 0
+
+
+@pytest.mark.parametrize("M,n,K", [(256, 256, 512), (300, 384, 136)])
+def test_fc1_exact_on_integer_inputs(sw, M, n, K):
+    """Integer X, W in [-3, 3]: every product and partial sum is an integer
+    below 2^24, so the tensor cores' fp32 accumulation is exact whatever its
+    order.  The stored fc1 must then equal the oracle's once-rounded exact value
+    bit for bit -- any misplaced row, column, gate/up pairing or K slab shows --
+    and y (computed from the exact fp32 accumulators) is within one bf16 step."""
+    g = torch.Generator().manual_seed(M * 7 + K)
+    X = torch.randint(-3, 4, (M, K), generator=g).to(torch.bfloat16)
+    Wt = torch.randint(-3, 4, (2 * n, K), generator=g).to(torch.bfloat16)
+    y, fc1 = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda(), return_fc1=True)
+    torch.cuda.synchronize()
+    y_or, fc1_or = oracle.fc1_swiglu_fwd(X, Wt, want_fc1=True)
+    assert torch.equal(fc1.cpu().view(torch.int16), fc1_or.view(torch.int16))
+    d = (bf16_ordered(y.cpu()) - bf16_ordered(y_or)).abs()
+    assert int(d.max()) <= 1
