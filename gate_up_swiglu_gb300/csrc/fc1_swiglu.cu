@@ -256,7 +256,8 @@ __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m2, int tiles_
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fc1_swiglu_pair_kernel(const __grid_constant__ CUtensorMap tm_x,
-                           const __grid_constant__ CUtensorMap tm_w, __nv_bfloat16 *__restrict__ y,
+                           const __grid_constant__ CUtensorMap tm_wg,
+                           const __grid_constant__ CUtensorMap tm_wu, __nv_bfloat16 *__restrict__ y,
                            __nv_bfloat16 *__restrict__ x_out, int M, int n, int K) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -276,7 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kblocks = (K + BK - 1) / BK;
     const int tiles_m2 = (M + PAIR_M - 1) / PAIR_M;
-    const int tiles_n = n / BN;
+    const int tiles_n = (n + BN - 1) / BN;  // the last column tile may be ragged
     const int tiles = tiles_m2 * tiles_n;
     const int cluster_id = blockIdx.x >> 1, clusters = gridDim.x >> 1;
 
@@ -293,7 +294,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_wg)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_wu)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -315,7 +317,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int m0, j0;
             pair_tile_coords(t, tiles_m2, tiles_n, m0, j0);
             const int my_m0 = m0 + BM * (int)rank;
-            const int w_row = leader ? j0 : n + j0;
+            // the gate and up halves of W have tensor maps of their own, each
+            // n rows long, so a ragged last column tile reads zeros past row n
+            // instead of rows of the other half
+            const CUtensorMap *wmap = leader ? &tm_wg : &tm_wu;
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int s = it % STAGES2;
                 if (!mbar_wait(empty0 + 8 * s, ((it / STAGES2) & 1) ^ 1)) {
@@ -325,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint32_t full_leader = map_to_rank(full0 + 8 * s, 0);
                 if (leader) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE2_BYTES);
                 tma_load_2d_pair(sa + s * A_BYTES, &tm_x, full_leader, kb * BK, my_m0);
-                tma_load_2d_pair(sb + s * B2_BYTES, &tm_w, full_leader, kb * BK, w_row);
+                tma_load_2d_pair(sb + s * B2_BYTES, wmap, full_leader, kb * BK, j0);
             }
         }
         // the leader's full barriers count both CTAs' bytes: once their last
@@ -412,7 +417,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                        if (j0 + c + 8 * q < n)  // n % 8 == 0: a 16-byte store is all in or all out
+                            store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
                     if (x_out != nullptr) {
                         uint32_t pg[16], pu[16];
 #pragma unroll
@@ -424,8 +430,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         __nv_bfloat16 *xu = xg + n;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-                            store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+                            if (j0 + c + 8 * q < n) {
+                                store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+                                store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+                            }
                         }
                     }
                 }
@@ -499,8 +507,7 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     if (dtype != SWIGLU_BF16) return SWIGLU_ERR_DTYPE;
     if (M < 0 || n < 0 || K < 0) return SWIGLU_ERR_SHAPE;
     if (M == 0 || n == 0) return SWIGLU_OK;
-    if (K == 0 || n % BN != 0 || K % 8 != 0 || M > INT32_MAX || K > INT32_MAX ||
-        2 * n > INT32_MAX || n / BN > 65535)
+    if (K == 0 || n % 8 != 0 || K % 8 != 0 || M > INT32_MAX || K > INT32_MAX || 2 * n > INT32_MAX)
         return SWIGLU_ERR_SHAPE;
     if (x_in == nullptr || w == nullptr || y == nullptr) return SWIGLU_ERR_NULL;
     if (((uintptr_t)x_in | (uintptr_t)w | (uintptr_t)y | (uintptr_t)x_out) % 16 != 0)
@@ -515,8 +522,10 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     EncodeTiled enc;
     cudaError_t e = encoder(enc);
     if (e != cudaSuccess) return fail(e);
-    CUtensorMap tm_x, tm_w;
-    if (!make_map(enc, &tm_x, x_in, M, K) || !make_map(enc, &tm_w, w, 2 * n, K))
+    CUtensorMap tm_x, tm_wg, tm_wu;
+    const char *w_up = static_cast<const char *>(w) + (size_t)n * K * 2;
+    if (!make_map(enc, &tm_x, x_in, M, K) || !make_map(enc, &tm_wg, w, n, K) ||
+        !make_map(enc, &tm_wu, w_up, n, K))
         return fail(cudaErrorInvalidValue);
     static std::atomic<bool> attr_set{false};
     if (!attr_set.load()) {
@@ -529,12 +538,12 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
-    const int64_t tiles = ((M + PAIR_M - 1) / PAIR_M) * (n / BN);  // 256-row pair tiles
+    const int64_t tiles = ((M + PAIR_M - 1) / PAIR_M) * ((n + BN - 1) / BN);  // 256 x 128 tiles
     if (tiles > INT32_MAX) return SWIGLU_ERR_SHAPE;
     const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
     const dim3 grid((unsigned)(2 * (pairs > 0 ? pairs : 1)));
     fc1_swiglu_pair_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tm_x, tm_w, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
+        tm_x, tm_wg, tm_wu, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
         (int)n, (int)K);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : fail(e);

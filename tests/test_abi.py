@@ -203,7 +203,7 @@ def test_fc1_rejections(sw):
     assert f(dt=F32) == -2
     assert f(M=-1) == -3
     assert f(M=0, x=None) == 0
-    assert f(n=100) == -3          # n must be a multiple of 128
+    assert f(n=100) == -3          # n must be a multiple of 8
     assert f(K=70) == -3           # K must be a multiple of 8
     assert f(K=0) == -3
     assert f(x=None) == -1

@@ -73,7 +73,8 @@ def _inputs(M, n, K, seed):
 
 
 @pytest.mark.parametrize("M,n,K", [(128, 128, 64), (256, 256, 512), (200, 384, 72),
-                                   (1, 128, 8), (333, 128, 1000)])
+                                   (1, 128, 8), (333, 128, 1000), (260, 200, 96), (64, 8, 64),
+                                   (130, 136, 128)])
 def test_fc1_small_against_oracle(sw, M, n, K):
     X, Wt = _inputs(M, n, K, seed=M + n + K)
     y, fc1 = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda(), return_fc1=True)
@@ -129,7 +130,7 @@ def test_fc1_module_gradients(sw, in_place):
     assert sw.fc1_timeout_flag() == 0
 
 
-@pytest.mark.parametrize("M,n,K", [(256, 256, 512), (300, 384, 136)])
+@pytest.mark.parametrize("M,n,K", [(256, 256, 512), (300, 384, 136), (257, 200, 64)])
 def test_fc1_exact_on_integer_inputs(sw, M, n, K):
     """Integer X, W in [-3, 3]: every product and partial sum is an integer
     below 2^24, so the tensor cores' fp32 accumulation is exact whatever its
