@@ -73,21 +73,29 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 }
 
 // Launch policy, chosen by sweeping pack width, unroll and resident CTAs per
-// SM over the Megatron-shape, large-FFN and Llama-like bf16 workloads on a
-// GB300: the forward is fastest with one 32-byte pack per operand in flight
+// SM on a GB300.  Over the Megatron-shape, large-FFN and Llama-like bf16
+// workloads the forward is fastest with one 32-byte pack per operand in flight
 // and 4 CTAs of 256 threads per SM, both backward forms with two 16-byte packs
-// and 3 CTAs per SM.  Filling the SM with more CTAs lost 5-10 %.
+// and 3 CTAs per SM (filling the SM with more CTAs lost 5-10 %).  Narrow packs
+// (4 bytes or less: odd n, misaligned rows) want more threads instead: four
+// packs in flight and 8 (forward) / 6 (backward) CTAs per SM, 6-8 % faster than
+// eight packs at 4 / 3 CTAs on the odd-width fp32 workload.
 struct Policy {
     int max_pack_bytes;
     int max_ctas_per_sm;
+    int max_ctas_per_sm_narrow;  // packs of 4 bytes or less
 };
-constexpr Policy kFwdPolicy = {32, 4};
-constexpr Policy kBwdPolicy = {16, 3};
+constexpr Policy kFwdPolicy = {32, 4, 8};
+constexpr Policy kBwdPolicy = {16, 3, 6};
+
+constexpr int ctas_cap(const Policy &p, int pack_bytes) {
+    return pack_bytes <= 4 ? p.max_ctas_per_sm_narrow : p.max_ctas_per_sm;
+}
 
 // Packs in flight per operand per thread: one 32-byte pack, two 16-byte
-// packs, four 8-byte packs, else eight.
+// packs, else four.
 constexpr int unroll_for(int pack_bytes) {
-    return pack_bytes >= 32 ? 1 : (pack_bytes >= 16 ? 2 : (pack_bytes >= 8 ? 4 : 8));
+    return pack_bytes >= 32 ? 1 : (pack_bytes >= 16 ? 2 : 4);
 }
 
 // Cache behaviour: inputs of the out-of-place kernels go through the
@@ -199,7 +207,7 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm > kFwdPolicy.max_ctas_per_sm) per_sm = kFwdPolicy.max_ctas_per_sm;
+    if (per_sm > ctas_cap(kFwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kFwdPolicy, E::kBytes * VEC);
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -258,7 +266,7 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm > kBwdPolicy.max_ctas_per_sm) per_sm = kBwdPolicy.max_ctas_per_sm;
+    if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -283,7 +291,7 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm > kBwdPolicy.max_ctas_per_sm) per_sm = kBwdPolicy.max_ctas_per_sm;
+    if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     int64_t grid = (int64_t)d.sms * per_sm;
     if (grid > a.rows) grid = a.rows;
     kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(bwd_params(a, VEC));
