@@ -178,3 +178,64 @@ def test_empty_and_workspace_errors(sw):
     sw.swiglu_gateup_weighted_bwd(torch.empty(32, 0, device="cuda"), torch.empty(32, 0, device="cuda"),
                                   torch.ones(32, device="cuda"), dw=dw)
     assert torch.equal(dw, torch.zeros_like(dw))
+
+
+LAYOUTS = [
+    # (dtype, rows, n, x_pad, dy_pad, dx_pad, misalign)
+    ("bf16", 70, 4100, 0, 0, 0, 0),      # 8-byte packs
+    ("bf16", 50, 2050, 2, 2, 6, 0),      # 4-byte packs, padded strides
+    ("bf16", 33, 999, 0, 0, 0, 0),       # single elements
+    ("bf16", 40, 2048, 0, 0, 0, 1),      # misaligned base pointers
+    ("f32", 45, 1026, 0, 0, 0, 0),       # 8-byte packs
+    ("f32", 37, 3000, 4, 4, 8, 0),       # 16-byte packs with padding
+    ("f32", 21, 5001, 1, 3, 1, 1),       # odd n, odd strides, misaligned
+    ("bf16", 600, 40, 0, 0, 0, 0),       # many short rows (row groups, tiles of one)
+]
+
+
+def _guard(rows, cols, pad, mis, dt, fill):
+    buf = torch.full((64 + mis + rows * (cols + pad) + 64,), fill, dtype=dt, device="cuda")
+    return buf, buf[64 + mis: 64 + mis + rows * (cols + pad)].view(rows, cols + pad)[:, :cols]
+
+
+@pytest.mark.parametrize("case", LAYOUTS, ids=[f"{c[0]}-r{c[1]}-n{c[2]}-p{c[3]}{c[4]}{c[5]}-m{c[6]}"
+                                               for c in LAYOUTS])
+def test_bias_and_weighted_layouts(sw, case):
+    dts, rows, n, xp, dyp, dxp, mis = case
+    dt = torch.float32 if dts == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(rows + n)
+    x_c = (torch.randn(rows, 2 * n, generator=g) * 3).to(dt)
+    dy_c = torch.randn(rows, n, generator=g).to(dt)
+    bias_c = (torch.randn(2 * n, generator=g) * 0.5).to(dt)
+    w_c = torch.rand(rows, generator=g)
+    xb, x = _guard(rows, 2 * n, xp, mis, dt, float("nan"))
+    dyb, dy = _guard(rows, n, dyp, mis, dt, float("nan"))
+    dxb, dx = _guard(rows, 2 * n, dxp, mis, dt, -7.0)
+    x.copy_(x_c)
+    dy.copy_(dy_c)
+    dxb0 = dxb.clone()
+    bias, wts = bias_c.cuda(), w_c.cuda()
+    # bias backward into the guarded dx, and its forward
+    _, db = sw.swiglu_gateup_bias_bwd(dy, x, bias, dx)
+    y = sw.swiglu_gateup_bias_fwd(x, bias)
+    torch.cuda.synchronize()
+    rdx, _ = oracle.bias_bwd(dy_c, x_c, bias_c)
+    assert_parity(dx, rdx, "bias dx")
+    assert_parity(y, oracle.bias_fwd(x_c, bias_c), "bias fwd")
+    dx64, db64 = oracle.bias_bwd(dy_c.double(), x_c.double(), bias_c.double())
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), "bias dbias")
+    dx.fill_(-7.0)
+    assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                       dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"
+    # weighted backward into the same guarded dx, and its forward
+    _, dw = sw.swiglu_gateup_weighted_bwd(dy, x, wts, dx)
+    yw = sw.swiglu_gateup_weighted_fwd(x, wts)
+    torch.cuda.synchronize()
+    rdx, _ = oracle.weighted_bwd(dy_c, x_c, w_c)
+    assert_parity(dx, rdx, "weighted dx")
+    assert_parity(yw, oracle.weighted_fwd(x_c, w_c), "weighted fwd")
+    t = dy_c.double() * oracle.fwd(x_c.double())
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, "weighted dw")
+    dx.fill_(-7.0)
+    assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                       dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"
