@@ -77,6 +77,12 @@ def load(path: str = None):
         lib.oracle_swiglu_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                                ctypes.c_int]
         lib.oracle_swiglu_bias_bwd.restype = ctypes.c_int
+        lib.oracle_swiglu_weighted_bias_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64,
+                                                        ctypes.c_int]
+        lib.oracle_swiglu_weighted_bias_fwd.restype = ctypes.c_int
+        lib.oracle_swiglu_weighted_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64,
+                                                        i64, i64, i64, ctypes.c_int]
+        lib.oracle_swiglu_weighted_bias_bwd.restype = ctypes.c_int
         lib.oracle_fc1_swiglu_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_int]
         lib.oracle_fc1_swiglu_fwd.restype = ctypes.c_int
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
@@ -231,6 +237,45 @@ def bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor, dx: torch.Te
     if rc != 0:
         raise ValueError("oracle_swiglu_bias_bwd rejected its arguments")
     return dx, dbias
+
+
+def weighted_bias_fwd(x: torch.Tensor, bias: torch.Tensor, w: torch.Tensor, lib=None) -> torch.Tensor:
+    """y = w[r] * silu(g + bias[:n]) * (u + bias[n:])."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(bias, "bias", x.dtype, 2 * n)
+    _vec(w, "w", torch.float32, rows)
+    y = torch.empty((rows, n), dtype=x.dtype)
+    rc = lib.oracle_swiglu_weighted_bias_fwd(x.data_ptr(), bias.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                             rows, n, x.stride(0), y.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_weighted_bias_fwd rejected its arguments")
+    return y
+
+
+def weighted_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor, w: torch.Tensor,
+                      lib=None):
+    """Returns (dx, dbias, dw)."""
+    lib = lib or load()
+    _rowmajor(x, "x")
+    _rowmajor(dy, "dy")
+    rows, two_n = x.shape
+    n = two_n // 2
+    _vec(bias, "bias", x.dtype, 2 * n)
+    _vec(w, "w", torch.float32, rows)
+    dx = torch.empty((rows, 2 * n), dtype=x.dtype)
+    dbias = torch.empty(2 * n, dtype=x.dtype)
+    dw = torch.empty(rows, dtype=torch.float32)
+    acc = torch.empty(2 * n, dtype=torch.float64)
+    rc = lib.oracle_swiglu_weighted_bias_bwd(dy.data_ptr(), x.data_ptr(), bias.data_ptr(),
+                                             w.data_ptr(), dx.data_ptr(), dbias.data_ptr(),
+                                             dw.data_ptr(), acc.data_ptr(), rows, n, dy.stride(0),
+                                             x.stride(0), dx.stride(0), _CODE[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle_swiglu_weighted_bias_bwd rejected its arguments")
+    return dx, dbias, dw
 
 
 def fc1_swiglu_fwd(X: torch.Tensor, Wt: torch.Tensor, want_fc1: bool = False, lib=None):

@@ -322,3 +322,52 @@ int oracle_fc1_swiglu_fwd(const void *X, const void *W, void *y, void *x_out, do
     }
     return ORACLE_OK;
 }
+
+/* ---- per-token weights and bias together ------------------------------------ */
+/* Megatron's routed-expert activation with a bias (the weighted_bias_swiglu_impl
+ * the page names in §Known issues 2, bias given): both of the above at once,
+ *   y = w[r] * silu(g + bias[j]) * (u + bias[n + j])
+ *   dx = the plain backward at the shifted values with dy scaled by w[r]
+ *   dw[r] = sum_j dy * silu(g + bias[j]) * (u + bias[n + j])
+ *   dbias[k] = sum_r dx[r, k]   (exact, before rounding)
+ * `acc` is caller scratch of 2n doubles. */
+int oracle_swiglu_weighted_bias_fwd(const void *x, const void *bias, const float *w, void *y,
+                                    int64_t rows, int64_t n, int64_t sx, int64_t sy, int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double wr = (double)w[r];
+        for (int64_t j = 0; j < n; ++j) {
+            double g = load_elem(x, r * sx + j, dtype) + load_elem(bias, j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);
+            store_elem(y, r * sy + j, dtype, wr * swiglu_fwd_pair(g, u));
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_swiglu_weighted_bias_bwd(const void *dy, const void *x, const void *bias,
+                                    const float *w, void *dx, void *dbias, float *dw, double *acc,
+                                    int64_t rows, int64_t n, int64_t sdy, int64_t sx, int64_t sdx,
+                                    int dtype) {
+    if (check_args(rows, n, dtype)) return ORACLE_BAD_ARG;
+    for (int64_t k = 0; k < 2 * n; ++k) acc[k] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        double wr = (double)w[r];
+        double sum = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            double d = load_elem(dy, r * sdy + j, dtype);
+            double g = load_elem(x, r * sx + j, dtype) + load_elem(bias, j, dtype);
+            double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);
+            double dg, du;
+            sum += d * swiglu_fwd_pair(g, u);
+            swiglu_bwd_pair(d * wr, g, u, &dg, &du);
+            acc[j] += dg;
+            acc[n + j] += du;
+            store_elem(dx, r * sdx + j, dtype, dg);
+            store_elem(dx, r * sdx + n + j, dtype, du);
+        }
+        dw[r] = (float)sum;
+    }
+    for (int64_t k = 0; k < 2 * n; ++k) store_elem(dbias, k, dtype, acc[k]);
+    return ORACLE_OK;
+}

@@ -356,6 +356,36 @@ def pin_bias(lib):
                            torch.tensor([oracle.bf16_from_double(float(v), lib=lib) for v in db64]))
 
 
+def pin_weighted_bias(lib):
+    """Weights and bias together: torch float64 autograd of
+    w[:, None] * F.silu(a + bias[:n]) * (b + bias[n:]) gives y and the gradients
+    of x, bias and w; w = 1 gives the bias-only form, zero bias the
+    weighted-only form."""
+    for seed, (rows, n) in enumerate([(9, 13), (1, 2), (30, 5)]):
+        x = _rand((rows, 2 * n), 190 + seed, 3.0)
+        dy = _rand((rows, n), 200 + seed)
+        bias = _rand((2 * n,), 210 + seed)
+        w = _rand((rows,), 220 + seed).float()
+        a, b = [t.clone().requires_grad_(True) for t in x.chunk(2, dim=-1)]
+        bt = bias.clone().requires_grad_(True)
+        wt = w.double().clone().requires_grad_(True)
+        ref = wt[:, None] * F.silu(a + bt[:n]) * (b + bt[n:])
+        ref.backward(dy)
+        y = oracle.weighted_bias_fwd(x, bias, w, lib=lib)
+        dx, db, dw = oracle.weighted_bias_bwd(dy, x, bias, w, lib=lib)
+        assert torch.allclose(y, ref.detach(), rtol=1e-12, atol=1e-300)
+        assert torch.allclose(dx[:, :n], a.grad, rtol=1e-11, atol=1e-13)
+        assert torch.allclose(dx[:, n:], b.grad, rtol=1e-11, atol=1e-300)
+        assert torch.allclose(db, bt.grad, rtol=1e-11, atol=1e-13)
+        assert torch.allclose(dw.double(), wt.grad, rtol=2e-7, atol=1e-30)
+        one, zero = torch.ones(rows), torch.zeros(2 * n, dtype=F64)
+        assert torch.equal(oracle.weighted_bias_fwd(x, bias, one, lib=lib), oracle.bias_fwd(x, bias, lib=lib))
+        assert torch.equal(oracle.weighted_bias_bwd(dy, x, bias, one, lib=lib)[1],
+                           oracle.bias_bwd(dy, x, bias, lib=lib)[1])
+        assert torch.equal(oracle.weighted_bias_bwd(dy, x, zero, w, lib=lib)[2],
+                           oracle.weighted_bwd(dy, x, w, lib=lib)[1])
+
+
 def pin_fc1_swiglu(lib):
     """linear_fc1 then the activation: equals torch float64 matmul X @ W.T
     followed by F.silu(gate) * up, and its fc1 output equals that matmul; with
@@ -377,7 +407,7 @@ def pin_fc1_swiglu(lib):
 PINS = [pin_zero_gate, pin_saturation, pin_stationary_point, pin_finite_differences,
         pin_torch_two_tensor, pin_bf16_rounding_brute, pin_rounding_matches_torch,
         pin_bf16_all_gates, pin_strided_layouts, pin_two_tensor_form, pin_weighted, pin_bias,
-        pin_fc1_swiglu]
+        pin_fc1_swiglu, pin_weighted_bias]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -417,6 +447,8 @@ MUTATIONS = {
     "weighted_grad_unscaled": ("swiglu_bwd_pair(d * wr, g, u, &dg, &du);", "swiglu_bwd_pair(d, g, u, &dg, &du);"),
     "bias_halves_swapped": ("double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, n + j, dtype);\n            store_elem(y",
                             "double u = load_elem(x, r * sx + n + j, dtype) + load_elem(bias, j, dtype);\n            store_elem(y"),
+    "weighted_bias_dw_unshifted": ("sum += d * swiglu_fwd_pair(g, u);\n            swiglu_bwd_pair(d * wr, g, u, &dg, &du);\n            acc[j] += dg;",
+                                   "sum += d * swiglu_fwd_pair(g - load_elem(bias, j, dtype), u);\n            swiglu_bwd_pair(d * wr, g, u, &dg, &du);\n            acc[j] += dg;"),
     "fc1_weight_transposed": ("load_elem(W, c * K + k, dtype)", "load_elem(W, k * 2 * n + c, dtype)"),
     "fc1_halves_swapped": ("store_elem(y, m * n + j, dtype, swiglu_fwd_pair(acc[j], acc[n + j]));",
                            "store_elem(y, m * n + j, dtype, swiglu_fwd_pair(acc[n + j], acc[j]));"),
