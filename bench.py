@@ -136,7 +136,7 @@ def stored_traffic(kernel_key: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 25 ms in the background."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -156,7 +156,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "25"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -467,6 +467,13 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
     bf = _event_ms(lambda: sw.swiglu_gateup_bias_fwd(x, bias, y, stream=stream), stream, reps)
     bb = _event_ms(lambda: sw.swiglu_gateup_bias_bwd(dy, x, bias, dx, dbias, ws, stream=stream),
                    stream, reps)
+    del ws
+    wsb = torch.empty(max(16, sw.weighted_bias_bwd_workspace_bytes(w.rows, n)), dtype=torch.uint8,
+                      device=dev)
+    wbf = _event_ms(lambda: sw.swiglu_gateup_weighted_bias_fwd(x, bias, wts, y, stream=stream),
+                    stream, reps)
+    wbb = _event_ms(lambda: sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts, dx, dbias, dw, wsb,
+                                                               stream=stream), stream, reps)
     del y, dx, dw, dbias
 
     def row(f_ms, b_ms, extra_note):
@@ -485,9 +492,11 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
         "fc1_swiglu_tcgen05": fc1,
         "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "
                                           "(one CTA per row); GB/s on the plain algorithmic bytes"),
-        "bias": row(bf, bb, f"[2n] bias; bwd includes the column-sum pass over a "
-                            f"{ws.numel() / 2**20:.1f} MiB workspace and the dbias reduction; "
-                            "GB/s on the plain algorithmic bytes"),
+        "bias": row(bf, bb, "[2n] bias; bwd includes the column-sum pass over a workspace and "
+                            "the dbias reduction; GB/s on the plain algorithmic bytes"),
+        "weighted_bias": row(wbf, wbb, f"[2n] bias and fp32 per-row weights; bwd returns dx, "
+                                       f"dbias and dw ({wsb.numel() / 2**20:.1f} MiB workspace); "
+                                       "GB/s on the plain algorithmic bytes"),
         "silu_mul_separate_tensors": {
             "layout": "gate and up as two contiguous [rows, n] tensors", "reps": reps,
             "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),

@@ -35,7 +35,8 @@ STATUS = {0: "SWIGLU_OK", -1: "SWIGLU_ERR_NULL", -2: "SWIGLU_ERR_DTYPE", -3: "SW
 EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
            "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-           "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
+           "swiglu_gateup_weighted_bias_fwd", "swiglu_gateup_weighted_bias_bwd_workspace_size",
+           "swiglu_gateup_weighted_bias_bwd", "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
            "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
 
 
@@ -75,6 +76,14 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_gateup_bias_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32,
                                                    i32, vp]
     lib.swiglu_gateup_bias_bwd_noalloc.restype = i32
+    lib.swiglu_gateup_weighted_bias_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
+    lib.swiglu_gateup_weighted_bias_fwd.restype = i32
+    lib.swiglu_gateup_weighted_bias_bwd_workspace_size.argtypes = [i64, i64,
+                                                                   ctypes.POINTER(ctypes.c_size_t)]
+    lib.swiglu_gateup_weighted_bias_bwd_workspace_size.restype = i32
+    lib.swiglu_gateup_weighted_bias_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                                    i64, i64, i64, i64, i64, i32, i32, vp]
+    lib.swiglu_gateup_weighted_bias_bwd.restype = i32
     lib.swiglu_fc1_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp]
     lib.swiglu_fc1_fwd.restype = i32
     lib.swiglu_fc1_timeout_flag.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -331,6 +340,75 @@ def swiglu_gateup_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
     return dx, dbias
 
 
+def swiglu_gateup_weighted_bias_fwd(x: torch.Tensor, bias: torch.Tensor, w: torch.Tensor,
+                                    y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """y = w[row] * silu(gate + bias[:n]) * (up + bias[n:]); bias: [2n] in x's
+    dtype, w: fp32, one weight per row of x."""
+    if y is None:
+        y = torch.empty((*x.shape[:-1], x.shape[-1] // 2), dtype=x.dtype, device=x.device)
+    _check_cuda(x, y, bias)
+    rows, two_n, sx = _rows_view(x, "x")
+    yrows, n, sy = _rows_view(y, "y")
+    if yrows != rows or 2 * n != two_n:
+        raise ValueError("y must be [..., n] with the rows of x")
+    _vector(bias, "bias", two_n, x.dtype)
+    _vector(w, "w", rows, torch.float32)
+    with torch.cuda.device(x.device):
+        st = lib.swiglu_gateup_weighted_bias_fwd(x.data_ptr(), bias.data_ptr(), w.data_ptr(),
+                                                 y.data_ptr(), rows, n, sx, sy, _DTYPE[x.dtype],
+                                                 _stream_handle(x, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_weighted_bias_fwd")
+    return y
+
+
+def weighted_bias_bwd_workspace_bytes(rows: int, n: int) -> int:
+    """Workspace the weighted bias backward needs on the current device."""
+    out = ctypes.c_size_t(0)
+    st = lib.swiglu_gateup_weighted_bias_bwd_workspace_size(rows, n, ctypes.byref(out))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_weighted_bias_bwd_workspace_size")
+    return int(out.value)
+
+
+def swiglu_gateup_weighted_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor,
+                                    w: torch.Tensor, dx=None, dbias=None, dw=None,
+                                    workspace: torch.Tensor = None, in_place: bool = False,
+                                    stream=None):
+    """Returns (dx, dbias, dw).  `workspace` (a CUDA byte tensor of at least
+    weighted_bias_bwd_workspace_bytes(rows, n)) is allocated here when not
+    given."""
+    if in_place:
+        dx = x
+    elif dx is None:
+        dx = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if dbias is None:
+        dbias = torch.empty_like(bias)
+    if dw is None:
+        dw = torch.empty(w.shape, dtype=torch.float32, device=x.device)
+    _check_cuda(dy, x, dx, bias, dbias)
+    rows, two_n, sx = _rows_view(x, "x")
+    dyrows, n, sdy = _rows_view(dy, "dy")
+    dxrows, dxcols, sdx = _rows_view(dx, "dx")
+    if dyrows != rows or 2 * n != two_n or dxrows != rows or dxcols != two_n:
+        raise ValueError("shapes must be dy [..., n], x [..., 2n], dx [..., 2n] over the same rows")
+    _vector(bias, "bias", two_n, x.dtype)
+    _vector(dbias, "dbias", two_n, x.dtype)
+    _vector(w, "w", rows, torch.float32)
+    _vector(dw, "dw", rows, torch.float32)
+    with torch.cuda.device(x.device):
+        if workspace is None:
+            workspace = torch.empty(max(16, weighted_bias_bwd_workspace_bytes(rows, n)),
+                                    dtype=torch.uint8, device=x.device)
+        st = lib.swiglu_gateup_weighted_bias_bwd(
+            dy.data_ptr(), x.data_ptr(), bias.data_ptr(), w.data_ptr(), dx.data_ptr(),
+            dbias.data_ptr(), dw.data_ptr(), workspace.data_ptr(), workspace.numel(), rows, n, sdy,
+            sx, sdx, _DTYPE[x.dtype], 1 if in_place else 0, _stream_handle(x, stream))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_weighted_bias_bwd")
+    return dx, dbias, dw
+
+
 def swiglu_fc1_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor = None,
                    x_out: torch.Tensor = None, return_fc1: bool = False, stream=None):
     """y = silu((x W^T)[..., :n]) * (x W^T)[..., n:] on the tensor cores, with W
@@ -366,7 +444,9 @@ def fc1_timeout_flag() -> int:
     return int(out.value)
 
 
-__all__ = ["swiglu_fc1_fwd", "fc1_timeout_flag", "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
-           "swiglu_gateup_bias_bwd", "bias_bwd_workspace_bytes",
-           "swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd", "status_string", "SwigluError", "lib",
+__all__ = ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
+           "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
+           "swiglu_gateup_bias_bwd", "bias_bwd_workspace_bytes", "swiglu_gateup_weighted_bias_fwd",
+           "swiglu_gateup_weighted_bias_bwd", "weighted_bias_bwd_workspace_bytes",
+           "swiglu_fc1_fwd", "fc1_timeout_flag", "status_string", "SwigluError", "lib",
            "SWIGLU_F32", "SWIGLU_BF16", "EXPORTS", "LIB_PATH"]

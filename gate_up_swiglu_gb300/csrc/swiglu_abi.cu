@@ -175,6 +175,7 @@ struct BwdArgs {
     float *partial = nullptr;                          // kBias workspace
     const float *w = nullptr;                          // kWeight
     float *dw = nullptr;
+    float *partial_dw = nullptr;                       // kBiasWeight workspace
 };
 
 // Row groups of the bias backward: enough (column tile, row group) CTAs to
@@ -184,7 +185,7 @@ struct BiasPlan {
     size_t workspace_bytes;
 };
 
-BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {
+BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {  // rows, n >= 1
     BiasPlan b;
     b.tiles = (n + swiglu::kBiasTileCols - 1) / swiglu::kBiasTileCols;
     int64_t groups = ((int64_t)sms * kBwdPolicy.max_ctas_per_sm) / b.tiles;
@@ -194,6 +195,18 @@ BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {
     b.groups = (rows + b.rows_per_group - 1) / b.rows_per_group;
     b.workspace_bytes = (size_t)b.groups * (size_t)(2 * n) * sizeof(float);
     return b;
+}
+
+// The weighted bias backward adds, after the column sums (from a 16-byte
+// boundary), one fp32 dw partial per (row, column tile).  False when the size
+// does not fit size_t.
+bool weighted_bias_workspace(int64_t rows, int64_t n, int sms, size_t &dw_offset, size_t &bytes) {
+    const BiasPlan b = bias_plan(rows, n, sms);
+    dw_offset = (b.workspace_bytes + 15) / 16 * 16;
+    size_t cells, dw_bytes;
+    if (__builtin_mul_overflow((size_t)rows, (size_t)b.tiles, &cells)) return false;
+    if (__builtin_mul_overflow(cells, sizeof(float), &dw_bytes)) return false;
+    return !__builtin_add_overflow(dw_offset, dw_bytes, &bytes);
 }
 
 template <typename E, int VEC, int MODE>
@@ -242,6 +255,7 @@ swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
     p.w = a.w;
     p.dw = a.dw;
     p.partial = a.partial;
+    p.partial_dw = a.partial_dw;
     p.rows = a.rows;
     p.dy_stride = a.dy.stride / vec;
     p.g_stride = a.g.stride / vec;
@@ -299,10 +313,11 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
-template <typename E, int VEC, bool IN_PLACE>
+template <typename E, int VEC, bool IN_PLACE, bool WEIGHTED>
 swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
-                                                 IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore>;
+                                                 IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore,
+                                                 WEIGHTED>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -316,13 +331,20 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)rgrid, swiglu::kThreads, 0, stream>>>(
         a.partial, b.groups, 2 * a.n, a.dbias);
     e = cudaGetLastError();
+    if (e != cudaSuccess || !WEIGHTED) return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+    int64_t wgrid = (a.rows + swiglu::kThreads - 1) / swiglu::kThreads;
+    if (wgrid > (int64_t)d.sms * 8) wgrid = (int64_t)d.sms * 8;
+    swiglu::swiglu_dw_reduce_kernel<<<(unsigned)wgrid, swiglu::kThreads, 0, stream>>>(
+        a.partial_dw, a.rows, (int32_t)b.tiles, a.dw);
+    e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
 template <typename E, int VEC, bool IN_PLACE>
 swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
     if (a.mode == swiglu::kWeight) return launch_bwd_weighted<E, VEC, IN_PLACE>(a, stream);
-    if (a.mode == swiglu::kBias) return launch_bwd_bias<E, VEC, IN_PLACE>(a, stream);
+    if (a.mode == swiglu::kBias) return launch_bwd_bias<E, VEC, IN_PLACE, false>(a, stream);
+    if (a.mode == swiglu::kBiasWeight) return launch_bwd_bias<E, VEC, IN_PLACE, true>(a, stream);
     return launch_bwd_plain<E, VEC, IN_PLACE>(a, stream);
 }
 
@@ -330,6 +352,7 @@ template <typename E, int VEC>
 swiglu_status_t launch_fwd_mode(const FwdArgs &a, cudaStream_t st) {
     if (a.mode == swiglu::kWeight) return launch_fwd<E, VEC, swiglu::kWeight>(a, st);
     if (a.mode == swiglu::kBias) return launch_fwd<E, VEC, swiglu::kBias>(a, st);
+    if (a.mode == swiglu::kBiasWeight) return launch_fwd<E, VEC, swiglu::kBiasWeight>(a, st);
     return launch_fwd<E, VEC, swiglu::kPlain>(a, st);
 }
 
@@ -340,7 +363,7 @@ template <typename E>
 swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const int64_t strides[3] = {a.g.stride, a.u.stride, a.y.stride};
     const void *ptrs[5] = {a.g.p, a.u.p, a.y.p, a.bias_g, a.bias_u};
-    const int np = a.mode == swiglu::kBias ? 5 : 3;
+    const int np = (a.mode & swiglu::kBias) ? 5 : 3;
     const int vec = pick_vec(E::kBytes, kFwdPolicy.max_pack_bytes, a.n, strides, 3, ptrs, np);
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);
@@ -354,7 +377,7 @@ template <typename E, bool IP>
 swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     const int64_t strides[5] = {a.dy.stride, a.g.stride, a.u.stride, a.dg.stride, a.du.stride};
     const void *ptrs[7] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p, a.bias_g, a.bias_u};
-    const int np = a.mode == swiglu::kBias ? 7 : 5;
+    const int np = (a.mode & swiglu::kBias) ? 7 : 5;
     const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, np);
     constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_bwd<E, 16, IP>(a, st);
@@ -419,6 +442,84 @@ swiglu_status_t gateup_bwd_args(const void *dy, const void *x, void *dx, int64_t
     a.rows = rows;
     a.n = n;
     return SWIGLU_OK;
+}
+
+// The bias backward, with per-token weights when w != nullptr (then dw is
+// written too and the workspace also holds the dw partials).
+swiglu_status_t bias_bwd_impl(const void *dy, const void *x, const void *bias, const float *w,
+                              void *dx, void *dbias, float *dw, void *workspace,
+                              size_t workspace_bytes, int64_t rows, int64_t n,
+                              int64_t dy_row_stride, int64_t x_row_stride, int64_t dx_row_stride,
+                              swiglu_dtype_t dtype, int in_place, swiglu_stream_t stream) {
+    swiglu_status_t st = check_common(dtype, rows, n);
+    if (st != SWIGLU_OK) return st;
+    if (n == 0 && rows == 0) return SWIGLU_OK;
+    const int eb = elem_bytes(dtype);
+    const bool weighted = w != nullptr;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) {  // every row sums nothing
+        if (!weighted) return SWIGLU_OK;
+        Span sws, sdws;
+        if (!span_of(w, 1, rows, rows, 4, sws) || !span_of(dw, 1, rows, rows, 4, sdws))
+            return SWIGLU_ERR_SHAPE;
+        if (overlaps(sws, sdws)) return SWIGLU_ERR_ALIAS;
+        cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)rows * sizeof(float), cs);
+        return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+    }
+    if (bias == nullptr || dbias == nullptr) return SWIGLU_ERR_NULL;
+    Span sbs, sdbs;
+    if (!span_of(bias, 1, 2 * n, 2 * n, eb, sbs) || !span_of(dbias, 1, 2 * n, 2 * n, eb, sdbs))
+        return SWIGLU_ERR_SHAPE;
+    if (overlaps(sbs, sdbs)) return SWIGLU_ERR_ALIAS;
+    if (rows == 0) {  // the sum over no rows
+        cudaError_t e = cudaMemsetAsync(dbias, 0, (size_t)(2 * n) * eb, cs);
+        return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+    }
+    if (workspace == nullptr) return SWIGLU_ERR_NULL;
+    BwdArgs a;
+    Span sp[3];
+    st = gateup_bwd_args(dy, x, dx, rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
+                         in_place, a, sp);
+    if (st != SWIGLU_OK) return st;
+    Span sws;
+    if (!span_of(workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1, sws))
+        return SWIGLU_ERR_SHAPE;
+    // dbias and the workspace are written: they overlap nothing; bias is read
+    // while dx is written
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(sdbs, sp[i]) || overlaps(sws, sp[i])) return SWIGLU_ERR_ALIAS;
+    if (overlaps(sws, sbs) || overlaps(sws, sdbs) || overlaps(sbs, sp[2])) return SWIGLU_ERR_ALIAS;
+    if (weighted) {
+        // dw is written: it overlaps nothing; w is read while dx, dbias and
+        // the workspace are written
+        Span sw, sdw;
+        if (!span_of(w, 1, rows, rows, 4, sw) || !span_of(dw, 1, rows, rows, 4, sdw))
+            return SWIGLU_ERR_SHAPE;
+        for (int i = 0; i < 3; ++i)
+            if (overlaps(sdw, sp[i])) return SWIGLU_ERR_ALIAS;
+        if (overlaps(sdw, sw) || overlaps(sdw, sbs) || overlaps(sdw, sdbs) || overlaps(sdw, sws))
+            return SWIGLU_ERR_ALIAS;
+        if (overlaps(sw, sp[2]) || overlaps(sw, sdbs) || overlaps(sw, sws)) return SWIGLU_ERR_ALIAS;
+    }
+    if ((uintptr_t)workspace % 16 != 0) return SWIGLU_ERR_WORKSPACE;
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    size_t need = bias_plan(rows, n, d.sms).workspace_bytes, dw_offset = 0;
+    if (weighted && !weighted_bias_workspace(rows, n, d.sms, dw_offset, need))
+        return SWIGLU_ERR_SHAPE;
+    if (workspace_bytes < need) return SWIGLU_ERR_WORKSPACE;
+    a.mode = weighted ? swiglu::kBiasWeight : swiglu::kBias;
+    a.bias_g = bias;
+    a.bias_u = static_cast<const char *>(bias) + n * eb;
+    a.dbias = dbias;
+    a.partial = static_cast<float *>(workspace);
+    if (weighted) {
+        a.w = w;
+        a.dw = dw;
+        a.partial_dw = reinterpret_cast<float *>(static_cast<char *>(workspace) + dw_offset);
+    }
+    return run_bwd(dtype, in_place != 0, a, stream);
 }
 
 }  // namespace
@@ -552,45 +653,64 @@ swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void
                                        int64_t x_row_stride, int64_t dx_row_stride,
                                        swiglu_dtype_t dtype, int in_place,
                                        swiglu_stream_t stream) {
+    return bias_bwd_impl(dy, x, bias, nullptr, dx, dbias, nullptr, workspace, workspace_bytes, rows,
+                         n, dy_row_stride, x_row_stride, dx_row_stride, dtype, in_place, stream);
+}
+
+swiglu_status_t swiglu_gateup_weighted_bias_fwd(const void *x, const void *bias, const float *w,
+                                                void *y, int64_t rows, int64_t n,
+                                                int64_t x_row_stride, int64_t y_row_stride,
+                                                swiglu_dtype_t dtype, swiglu_stream_t stream) {
     swiglu_status_t st = check_common(dtype, rows, n);
     if (st != SWIGLU_OK) return st;
-    if (n == 0) return SWIGLU_OK;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
     const int eb = elem_bytes(dtype);
-    if (bias == nullptr || dbias == nullptr) return SWIGLU_ERR_NULL;
-    Span sbs, sdbs;
-    if (!span_of(bias, 1, 2 * n, 2 * n, eb, sbs) || !span_of(dbias, 1, 2 * n, 2 * n, eb, sdbs))
+    if (x == nullptr || y == nullptr || bias == nullptr || w == nullptr) return SWIGLU_ERR_NULL;
+    if (x_row_stride < 2 * n || y_row_stride < n) return SWIGLU_ERR_STRIDE;
+    Span sxs, sys, sbs, sws;
+    if (!span_of(x, rows, 2 * n, x_row_stride, eb, sxs) ||
+        !span_of(y, rows, n, y_row_stride, eb, sys) || !span_of(bias, 1, 2 * n, 2 * n, eb, sbs) ||
+        !span_of(w, 1, rows, rows, 4, sws))
         return SWIGLU_ERR_SHAPE;
-    if (overlaps(sbs, sdbs)) return SWIGLU_ERR_ALIAS;
-    if (rows == 0) {  // the sum over no rows
-        cudaError_t e = cudaMemsetAsync(dbias, 0, (size_t)(2 * n) * eb,
-                                        reinterpret_cast<cudaStream_t>(stream));
-        return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
-    }
-    if (workspace == nullptr) return SWIGLU_ERR_NULL;
-    BwdArgs a;
-    Span sp[3];
-    st = gateup_bwd_args(dy, x, dx, rows, n, dy_row_stride, x_row_stride, dx_row_stride, dtype,
-                         in_place, a, sp);
-    if (st != SWIGLU_OK) return st;
-    Span sws;
-    if (!span_of(workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1, sws))
-        return SWIGLU_ERR_SHAPE;
-    // dbias and the workspace are written: they overlap nothing; bias is read
-    // while dx is written
-    for (int i = 0; i < 3; ++i)
-        if (overlaps(sdbs, sp[i]) || overlaps(sws, sp[i])) return SWIGLU_ERR_ALIAS;
-    if (overlaps(sws, sbs) || overlaps(sws, sdbs) || overlaps(sbs, sp[2])) return SWIGLU_ERR_ALIAS;
-    if ((uintptr_t)workspace % 16 != 0) return SWIGLU_ERR_WORKSPACE;
+    if (overlaps(sxs, sys) || overlaps(sbs, sys) || overlaps(sws, sys)) return SWIGLU_ERR_ALIAS;
+    const char *xb = static_cast<const char *>(x);
+    FwdArgs a{{x, x_row_stride}, {xb + n * eb, x_row_stride}, {y, y_row_stride}, rows, n};
+    a.mode = swiglu::kBiasWeight;
+    a.bias_g = bias;
+    a.bias_u = static_cast<const char *>(bias) + n * eb;
+    a.w = w;
+    return run_fwd(dtype, a, stream);
+}
+
+swiglu_status_t swiglu_gateup_weighted_bias_bwd_workspace_size(int64_t rows, int64_t n,
+                                                               size_t *bytes) {
+    if (bytes == nullptr) return SWIGLU_ERR_NULL;
+    if (rows < 0 || n < 0 || n > SWIGLU_MAX_N) return SWIGLU_ERR_SHAPE;
+    *bytes = 0;
+    if (rows == 0 || n == 0) return SWIGLU_OK;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (workspace_bytes < bias_plan(rows, n, d.sms).workspace_bytes) return SWIGLU_ERR_WORKSPACE;
-    a.mode = swiglu::kBias;
-    a.bias_g = bias;
-    a.bias_u = static_cast<const char *>(bias) + n * eb;
-    a.dbias = dbias;
-    a.partial = static_cast<float *>(workspace);
-    return run_bwd(dtype, in_place != 0, a, stream);
+    size_t off;
+    if (!weighted_bias_workspace(rows, n, d.sms, off, *bytes)) return SWIGLU_ERR_SHAPE;
+    return SWIGLU_OK;
+}
+
+swiglu_status_t swiglu_gateup_weighted_bias_bwd(
+    const void *dy, const void *x, const void *bias, const float *w, void *dx, void *dbias,
+    float *dw, void *workspace, size_t workspace_bytes, int64_t rows, int64_t n,
+    int64_t dy_row_stride, int64_t x_row_stride, int64_t dx_row_stride, swiglu_dtype_t dtype,
+    int in_place, swiglu_stream_t stream) {
+    if (w == nullptr || dw == nullptr) {  // the rest is checked in bias_bwd_impl
+        swiglu_status_t st = check_common(dtype, rows, n);
+        if (st != SWIGLU_OK) return st;
+        return rows == 0 ? bias_bwd_impl(dy, x, bias, nullptr, dx, dbias, nullptr, workspace,
+                                         workspace_bytes, rows, n, dy_row_stride, x_row_stride,
+                                         dx_row_stride, dtype, in_place, stream)
+                         : SWIGLU_ERR_NULL;
+    }
+    return bias_bwd_impl(dy, x, bias, w, dx, dbias, dw, workspace, workspace_bytes, rows, n,
+                         dy_row_stride, x_row_stride, dx_row_stride, dtype, in_place, stream);
 }
 
 swiglu_status_t swiglu_silu_mul_fwd(const void *a, const void *b, void *c, int64_t rows, int64_t n,
@@ -662,7 +782,7 @@ const char *swiglu_status_string(swiglu_status_t status) {
 
 int swiglu_last_cuda_error(void) { return g_last_cuda_error; }
 
-int swiglu_abi_version(void) { return 3; }
+int swiglu_abi_version(void) { return 4; }
 
 }  // extern "C"
 

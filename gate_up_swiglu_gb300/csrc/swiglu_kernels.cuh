@@ -305,7 +305,8 @@ __device__ __forceinline__ void store_pack(uint32_t *w, const float *v) {
 //   kPlain   silu(g) * u
 //   kBias    silu(g + bias_g[j]) * (u + bias_u[j])
 //   kWeight  w[r] * silu(g) * u            (w: fp32 per row)
-enum : int { kPlain = 0, kBias = 1, kWeight = 2 };
+//   kBiasWeight  both: w[r] * silu(g + bias_g[j]) * (u + bias_u[j])
+enum : int { kPlain = 0, kBias = 1, kWeight = 2, kBiasWeight = 3 };  // bit flags
 
 struct FwdParams {
     const void *g;
@@ -334,6 +335,7 @@ struct BwdParams {
     const float *w;      // kWeight: [rows]
     float *dw;           // kWeight: [rows]
     float *partial;      // kBias: [groups, 2n] fp32 column sums per row group
+    float *partial_dw;   // kBiasWeight: [rows, tiles] fp32 row sums per column tile
     int64_t rows;
     int64_t dy_stride;  // row strides, in packs
     int64_t g_stride;
@@ -371,7 +373,7 @@ __device__ __forceinline__ void advance(int64_t step_q, int32_t step_r, int32_t 
 }
 
 template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain>
-__global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     using L = Ld<B, LD>;
@@ -392,11 +394,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
             if (r[k] < p.rows) {
                 L::run(gp + (r[k] * p.g_stride + c[k]) * B, g[k]);
                 L::run(up + (r[k] * p.u_stride + c[k]) * B, u[k]);
-                if (MODE == kBias) {
+                if (MODE & kBias) {
                     Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_g) + (int64_t)c[k] * B, bg[k]);
                     Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_u) + (int64_t)c[k] * B, bu[k]);
                 }
-                if (MODE == kWeight) wr[k] = __ldg(p.w + r[k]);
+                if (MODE & kWeight) wr[k] = __ldg(p.w + r[k]);
             }
         }
 #pragma unroll
@@ -407,13 +409,13 @@ __global__ void __launch_bounds__(kThreads) swiglu_fwd_kernel(const FwdParams p)
 #pragma unroll
                 for (int i = 0; i < VEC; ++i) {
                     float gf = E::get(g[k], i), uf = E::get(u[k], i);
-                    if (MODE == kBias) {
+                    if (MODE & kBias) {
                         gf = __fadd_rn(gf, E::get(bg[k], i));
                         uf = __fadd_rn(uf, E::get(bu[k], i));
                     }
                     const Act act = activation<E, false>(gf);
                     float v = __fmul_rn(act.silu, uf);
-                    if (MODE == kWeight) v = __fmul_rn(v, wr[k]);
+                    if (MODE & kWeight) v = __fmul_rn(v, wr[k]);
                     yv[i] = __fmul_rn(v, act.scale);
                 }
                 store_pack<E, VEC>(o, yv);
@@ -506,7 +508,7 @@ template <typename E, int MODE>
 __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float uf, float bgf,
                                                      float buf, float wr) {
     float g_lo = 0.0f;
-    if (MODE == kBias) {
+    if (MODE & kBias) {
         if (E::kRootWindow)
             gf = two_sum(gf, bgf, g_lo);
         else
@@ -516,7 +518,7 @@ __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float u
     const Act act = activation<E, true>(gf, g_lo);
     BwdPair<E, MODE> o;
     o.dw_term = 0.0f;
-    if (MODE == kWeight) {
+    if (MODE & kWeight) {
         // dw[r] sums dy * silu(g) * u over the row; dy * w drives the gradient
         o.dw_term = __fmul_rn(__fmul_rn(__fmul_rn(df, act.silu), uf), act.scale);
         df = __fmul_rn(df, wr);
@@ -586,9 +588,18 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const Bwd
 // sums of its rows, in fp32, in partial[group][0, 2n).
 constexpr int kBiasTileCols = 2048;
 
-template <typename E, int VEC, bool IN_PLACE, int LD, int ST>
+// With WEIGHTED (per-token weights as well), each row's dw terms over the
+// tile's columns are summed across the CTA into partial_dw[row, tile]: every
+// thread parks its row sum in shared memory, and once per kDwBatch rows, after
+// one barrier, each warp finishes rows of the batch: a lane adds the sums of
+// threads lane, lane + 32, ... in order, then a shuffle tree adds the lanes.
+// The row loop itself carries no cross-thread step.
+template <typename E, int VEC, bool IN_PLACE, int LD, int ST, bool WEIGHTED = false>
 __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
                                                                       int64_t rows_per_group) {
+    constexpr int MODE = WEIGHTED ? kBiasWeight : kBias;
+    constexpr int kDwBatch = 32;
+    __shared__ float wpart[WEIGHTED ? kDwBatch : 1][WEIGHTED ? kThreads : 1];
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
@@ -604,19 +615,18 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     const int64_t r0 = group * rows_per_group;
     const int64_t r1 = min(p.rows, r0 + rows_per_group);
     int32_t c[PPT];
-    float bg[PPT][VEC], bu[PPT][VEC], ag[PPT][VEC], au[PPT][VEC];
+    // the bias stays in its packed storage form (half the registers for bf16)
+    // and is widened where it is used
+    uint32_t bg[PPT][NW], bu[PPT][NW];
+    float ag[PPT][VEC], au[PPT][VEC];
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
         c[k] = tile * (kBiasTileCols / VEC) + k * kThreads + threadIdx.x;
-        uint32_t wb[NW], wu[NW];
-        if (c[k] < p.nvec) {
-            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_g) + (int64_t)c[k] * B, wb);
-            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_u) + (int64_t)c[k] * B, wu);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-                bg[k][i] = E::get(wb, i);
-                bu[k][i] = E::get(wu, i);
-            }
+        for (int i = 0; i < NW; ++i) bg[k][i] = bu[k][i] = 0u;
+        if (c[k] < p.nvec) {
+            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_g) + (int64_t)c[k] * B, bg[k]);
+            Ld<B, kLdCached>::run(static_cast<const char *>(p.bias_u) + (int64_t)c[k] * B, bu[k]);
         }
 #pragma unroll
         for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
@@ -638,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
         for (int q = 0; q < RU; ++q) {
             const int64_t r = rb + q;
+            const float wr = (WEIGHTED && r < r1) ? __ldg(p.w + r) : 1.0f;
+            float rowsum = 0.0f;
 #pragma unroll
             for (int k = 0; k < PPT; ++k) {
                 if (r < r1 && c[k] < p.nvec) {
@@ -645,9 +657,11 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                     float gv[VEC], uv[VEC];
 #pragma unroll
                     for (int i = 0; i < VEC; ++i) {
-                        const BwdPair<E, kBias> o =
-                            bwd_pair<E, kBias>(E::get(d[q][k], i), E::get(g[q][k], i),
-                                               E::get(u[q][k], i), bg[k][i], bu[k][i], 1.0f);
+                        const BwdPair<E, MODE> o =
+                            bwd_pair<E, MODE>(E::get(d[q][k], i), E::get(g[q][k], i),
+                                              E::get(u[q][k], i), E::get(bg[k], i),
+                                              E::get(bu[k], i), wr);
+                        if (WEIGHTED) rowsum = __fadd_rn(rowsum, o.dw_term);
                         ag[k][i] = __fadd_rn(ag[k][i], o.dg);
                         au[k][i] = __fadd_rn(au[k][i], o.du);
                         gv[i] = o.dg;
@@ -657,6 +671,24 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                     store_pack<E, VEC>(ou, uv);
                     S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
                     S::run(static_cast<char *>(p.du) + (r * p.du_stride + c[k]) * B, ou);
+                }
+            }
+            if (WEIGHTED && r < r1) {  // r is the same for every thread of the CTA
+                const int slot = (int)((r - r0) % kDwBatch);
+                wpart[slot][threadIdx.x] = rowsum;
+                if (slot == kDwBatch - 1 || r == r1 - 1) {
+                    __syncthreads();
+                    const int lane = threadIdx.x & 31;
+                    for (int q = threadIdx.x >> 5; q <= slot; q += kThreads / 32) {
+                        float t = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < kThreads / 32; ++k) t = __fadd_rn(t, wpart[q][lane + 32 * k]);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+                        if (lane == 0) p.partial_dw[(r - slot + q) * tiles + tile] = t;
+                    }
+                    __syncthreads();  // wpart is refilled by the next batch
                 }
             }
         }
@@ -691,6 +723,17 @@ __global__ void __launch_bounds__(kThreads) swiglu_bias_reduce_kernel(const floa
             static_cast<uint32_t *>(dbias)[k] = w[0];
         else
             static_cast<unsigned short *>(dbias)[k] = (unsigned short)w[0];
+    }
+}
+
+// dw[r] = sum over column tiles of partial_dw[r, tile], in tile order.
+static __global__ void __launch_bounds__(kThreads)
+    swiglu_dw_reduce_kernel(const float *partial_dw, int64_t rows, int32_t tiles, float *dw) {
+    for (int64_t r = (int64_t)blockIdx.x * kThreads + threadIdx.x; r < rows;
+         r += (int64_t)gridDim.x * kThreads) {
+        float s = 0.0f;
+        for (int32_t t = 0; t < tiles; ++t) s = __fadd_rn(s, partial_dw[r * tiles + t]);
+        dw[r] = s;
     }
 }
 

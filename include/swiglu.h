@@ -179,6 +179,38 @@ swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void
                                        swiglu_stream_t stream);
 
 /*
+ * Per-token weights and bias together (Liger-Kernel Megatron SwiGLU page,
+ * §Scope and §Known issues 2: the MoE routed experts' weighted_bias_swiglu_impl
+ * takes both).  bias / dbias as in swiglu_gateup_bias_*, w / dw as in
+ * swiglu_gateup_weighted_*:
+ *   forward   y[r, j]  = w[r] * silu(g + bias[j]) * (u + bias[n + j])
+ *   backward  dx       = the bias backward with dy[r, :] scaled by w[r]
+ *             dbias[k] = sum_r dx[r, k]                      (as for the bias form)
+ *             dw[r]    = sum_j dy[r, j] * silu(g + bias[j]) * (u + bias[n + j])
+ * Both sums run in fp32 in a fixed order (deterministic).  The backward needs
+ * a device workspace of at least
+ * swiglu_gateup_weighted_bias_bwd_workspace_size(rows, n) bytes, 16-byte
+ * aligned: the bias form's column sums plus one fp32 partial of dw per row and
+ * 2048-column tile.  Aliasing: y / dx / dbias / dw / workspace may overlap
+ * neither bias nor w; dbias, dw and the workspace overlap nothing.
+ * With rows == 0 (n > 0) the backward sets dbias to zero; with n == 0
+ * (rows > 0) it sets dw to zero.
+ */
+swiglu_status_t swiglu_gateup_weighted_bias_fwd(const void *x, const void *bias, const float *w,
+                                                void *y, int64_t rows, int64_t n,
+                                                int64_t x_row_stride, int64_t y_row_stride,
+                                                swiglu_dtype_t dtype, swiglu_stream_t stream);
+
+swiglu_status_t swiglu_gateup_weighted_bias_bwd_workspace_size(int64_t rows, int64_t n,
+                                                               size_t *bytes);
+
+swiglu_status_t swiglu_gateup_weighted_bias_bwd(
+    const void *dy, const void *x, const void *bias, const float *w, void *dx, void *dbias,
+    float *dw, void *workspace, size_t workspace_bytes, int64_t rows, int64_t n,
+    int64_t dy_row_stride, int64_t x_row_stride, int64_t dx_row_stride, swiglu_dtype_t dtype,
+    int in_place, swiglu_stream_t stream);
+
+/*
  * Allocation-free bias backward.  The page has no counterpart: this is an
  * addition for callers that cannot hand the library any device memory -- for
  * example code running under an engine that plans all device memory ahead of

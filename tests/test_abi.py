@@ -35,8 +35,10 @@ def test_header_declares_expected_calls():
         ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
          "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
          "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
-         "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
-         "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version"])
+         "swiglu_gateup_weighted_bias_fwd", "swiglu_gateup_weighted_bias_bwd_workspace_size",
+         "swiglu_gateup_weighted_bias_bwd", "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd",
+         "swiglu_fc1_timeout_flag", "swiglu_status_string", "swiglu_last_cuda_error",
+         "swiglu_abi_version"])
 
 
 def test_library_exports_every_declared_symbol(sw):
@@ -56,7 +58,7 @@ def test_status_strings(sw):
         s = sw.status_string(code)
         assert s and s != "unknown status"
     assert sw.status_string(-99) == "unknown status"
-    assert sw.lib.swiglu_abi_version() == 3
+    assert sw.lib.swiglu_abi_version() == 4
     assert sw.lib.swiglu_last_cuda_error() == 0
 
 
@@ -194,6 +196,43 @@ def test_bias_rejections(sw):
     assert b(ws=BIAS) == -5              # workspace over bias
     assert b(bias=DX) == -5              # bias under the written dx
     assert b(ws=WS + 4) == -7            # misaligned workspace
+
+
+def test_weighted_bias_rejections(sw):
+    import ctypes
+
+    out = ctypes.c_size_t(123)
+    assert sw.lib.swiglu_gateup_weighted_bias_bwd_workspace_size(4, 0, ctypes.byref(out)) == 0
+    assert out.value == 0
+    assert sw.lib.swiglu_gateup_weighted_bias_bwd_workspace_size(4, -8, ctypes.byref(out)) == -3
+    assert sw.lib.swiglu_gateup_weighted_bias_bwd_workspace_size(4, 8, None) == -1
+    f = lambda **k: sw.lib.swiglu_gateup_weighted_bias_fwd(  # noqa: E731
+        X, k.get("bias", BIAS), k.get("w", W), k.get("y", Y), 4, 8, 16, 8, BF16, None)
+    assert f(bias=None) == -1
+    assert f(w=None) == -1
+    assert f(y=BIAS + 4) == -5           # y over bias
+    assert f(y=W + 4) == -5              # y over w
+    b = lambda **k: sw.lib.swiglu_gateup_weighted_bias_bwd(  # noqa: E731
+        DY, X, k.get("bias", BIAS), k.get("w", W), k.get("dx", DX), k.get("dbias", DBIAS),
+        k.get("dw", DW), k.get("ws", WS), k.get("wsb", 1 << 20), k.get("rows", 4), k.get("n", 8),
+        8, 16, 16, BF16, k.get("ip", 0), None)
+    assert b(rows=0, w=None, dw=None, dbias=None) == -1   # dbias still needed (set to zero)
+    assert b(n=0, rows=0) == 0
+    assert b(w=None) == -1
+    assert b(dw=None) == -1
+    assert b(bias=None) == -1
+    assert b(ws=None) == -1
+    assert b(dw=W + 4) == -5             # dw over w
+    assert b(dw=DBIAS) == -5             # dw over dbias
+    assert b(dw=WS + 64) == -5           # dw over the workspace
+    assert b(dw=X + 8) == -5             # dw over x
+    assert b(w=DX) == -5                 # w under the written dx
+    assert b(w=DBIAS) == -5              # w under the written dbias
+    assert b(w=WS) == -5                 # w under the workspace
+    assert b(bias=DX) == -5              # bias under the written dx
+    assert b(ws=DX + 16) == -5           # workspace over dx
+    assert b(ws=WS + 4) == -7            # misaligned workspace
+    assert b(ip=1, dx=DX) == -5          # the in-place contract still holds
 
 
 def test_fc1_rejections(sw):

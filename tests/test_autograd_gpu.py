@@ -84,3 +84,73 @@ def test_module_delegates_bias_to_fallback(ag):
     assert torch.allclose(out, megatron_like(x, bias, False, False))
     # without a bias the fused kernels run and agree with the oracle
     assert_parity(m(x), oracle.fwd(x.cpu()), "module fwd")
+
+
+@pytest.mark.parametrize("name,rows", [("tiny_f32", None), ("megatron_4096_bf16", 96),
+                                       ("odd_5503_f32", 40)])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_bias_and_weighted_autograd_match_oracle(ag, name, rows, in_place):
+    """Bias, per-token weights, and both, through autograd: every gradient the
+    graph asks for (input, bias, weights) against the oracle."""
+    w = W.WORKLOADS[name]
+    x_cpu, dy_cpu = W.make_inputs(w, "cpu", rows=rows)
+    r, n = x_cpu.shape[0], w.n
+    g = torch.Generator().manual_seed(21)
+    b_cpu = (torch.randn(2 * n, generator=g) * 0.5).to(x_cpu.dtype)
+    w_cpu = torch.rand(r, 1, generator=g)  # Megatron's [tokens, 1] routing weights
+    dy = dy_cpu.cuda()
+
+    leaf = x_cpu.cuda().requires_grad_(True)
+    bias = b_cpu.cuda().requires_grad_(True)
+    y = ag.bias_gate_up_swiglu(leaf * 1, bias, in_place)
+    assert_parity(y.detach(), oracle.bias_fwd(x_cpu, b_cpu), f"{name} bias fwd")
+    y.backward(dy)
+    rdx, _ = oracle.bias_bwd(dy_cpu, x_cpu, b_cpu)
+    assert_parity(leaf.grad, rdx, f"{name} bias dx")
+    import gate_up_swiglu_gb300 as sw
+
+    # the reductions (bounded against the oracle in the variant tests) are
+    # deterministic, so autograd must hand back exactly the kernels' sums
+    _, db_ref = sw.swiglu_gateup_bias_bwd(dy, x_cpu.cuda(), b_cpu.cuda())
+    assert_bitwise(bias.grad, db_ref, f"{name} autograd dbias is the kernel's")
+
+    for with_bias in (False, True):
+        leaf = x_cpu.cuda().requires_grad_(True)
+        wts = w_cpu.cuda().requires_grad_(True)
+        bias = b_cpu.cuda().requires_grad_(True) if with_bias else None
+        y = ag.weighted_gate_up_swiglu(leaf * 1, bias, wts, in_place)
+        y.backward(dy)
+        w32 = w_cpu.view(-1).cuda()
+        if with_bias:
+            assert_parity(y.detach(), oracle.weighted_bias_fwd(x_cpu, b_cpu, w_cpu.view(-1)),
+                          f"{name} weighted bias fwd")
+            rdx, _, _ = oracle.weighted_bias_bwd(dy_cpu, x_cpu, b_cpu, w_cpu.view(-1))
+            _, db_ref, dw_ref = sw.swiglu_gateup_weighted_bias_bwd(dy, x_cpu.cuda(), b_cpu.cuda(), w32)
+            assert_bitwise(bias.grad, db_ref, f"{name} autograd weighted dbias")
+        else:
+            assert_parity(y.detach(), oracle.weighted_fwd(x_cpu, w_cpu.view(-1)),
+                          f"{name} weighted fwd")
+            rdx, _ = oracle.weighted_bwd(dy_cpu, x_cpu, w_cpu.view(-1))
+            _, dw_ref = sw.swiglu_gateup_weighted_bwd(dy, x_cpu.cuda(), w32)
+        assert_parity(leaf.grad, rdx, f"{name} weighted dx (bias={with_bias})")
+        assert wts.grad.shape == (r, 1) and wts.grad.dtype == torch.float32
+        assert_bitwise(wts.grad.view(-1), dw_ref, f"{name} autograd dw (bias={with_bias})")
+
+
+def test_module_native_bias_and_weighted_module(ag):
+    w = W.WORKLOADS["megatron_4096_bf16"]
+    x_cpu, dy_cpu = W.make_inputs(w, "cpu", rows=64)
+    n = w.n
+    b_cpu = (torch.randn(2 * n, generator=torch.Generator().manual_seed(3)) * 0.5).to(torch.bfloat16)
+    x3 = x_cpu.cuda().view(16, 4, 2 * n)
+    m = ag.GateUpSwiGLU(native_bias=True)  # no fallback needed
+    y = m(x3, b_cpu.cuda())
+    assert y.shape == (16, 4, n)
+    assert_parity(y.detach().view(64, n), oracle.bias_fwd(x_cpu, b_cpu), "native bias module fwd")
+    mw = ag.WeightedGateUpSwiGLU()
+    wts = torch.rand(64, 1, generator=torch.Generator().manual_seed(4))
+    yw = mw(x3, None, wts.cuda())
+    assert_parity(yw.detach().view(64, n), oracle.weighted_fwd(x_cpu, wts.view(-1)),
+                  "weighted module fwd")
+    with pytest.raises(NotImplementedError):
+        mw(x3, None, wts.cuda(), True)

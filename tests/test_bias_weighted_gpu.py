@@ -10,6 +10,9 @@ longest chain),
 For dw, D = n / 256 (the columns one thread adds) + 5 (warp shuffle levels) +
 8 (warp partials).  For dbias, D = rows per row group + number of groups,
 from the same plan the library makes (2048-column tiles, 3 CTAs per SM).
+With weights and bias together, dw is summed per 2048-column tile (8 terms per
+thread, then the CTA's 5 + 8 levels) and the tiles are added in order:
+D = 21 + number of tiles.
 """
 import math
 
@@ -117,6 +120,86 @@ def test_bias_matches_oracle(sw, name, rows):
     assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(r, n), f"{name} dbias")
 
 
+def _wb_dw_depth(n):
+    return 21 + -(-n // 2048)
+
+
+def _check_weighted_bias(dy_c, x_c, bias_c, w_c, y, dx, db, dw, what):
+    """y, dx against the oracle elementwise; dbias and dw against the exact sums."""
+    rows, n = dy_c.shape
+    assert_parity(y, oracle.weighted_bias_fwd(x_c, bias_c, w_c), f"{what} fwd")
+    rdx, _, _ = oracle.weighted_bias_bwd(dy_c, x_c, bias_c, w_c)
+    assert_parity(dx, rdx, f"{what} dx")
+    x64, dy64, b64 = x_c.double(), dy_c.double(), bias_c.double()
+    dx64, db64, _ = oracle.weighted_bias_bwd(dy64, x64, b64, w_c)
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), f"{what} dbias")
+    t = dy64 * oracle.bias_fwd(x64, b64)
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), _wb_dw_depth(n), f"{what} dw")
+
+
+@pytest.mark.parametrize("name,rows", CASES)
+def test_weighted_bias_matches_oracle(sw, name, rows):
+    w_ = W.WORKLOADS[name]
+    x, dy = W.make_inputs(w_, "cpu", rows=rows)
+    r, n = x.shape[0], w_.n
+    g = torch.Generator().manual_seed(9)
+    bias = (torch.randn(2 * n, generator=g) * 0.5).to(x.dtype)
+    wts = torch.rand(r, generator=g)
+    xd, dyd, bd, wd = x.cuda(), dy.cuda(), bias.cuda(), wts.cuda()
+    y = sw.swiglu_gateup_weighted_bias_fwd(xd, bd, wd)
+    dx, db, dw = sw.swiglu_gateup_weighted_bias_bwd(dyd, xd, bd, wd)
+    xi = xd.clone()
+    dxi, dbi, dwi = sw.swiglu_gateup_weighted_bias_bwd(dyd, xi, bd, wd, in_place=True)
+    torch.cuda.synchronize()
+    _check_weighted_bias(dy, x, bias, wts, y, dx, db, dw, f"{name} weighted bias")
+    assert_bitwise(xi, dx, "weighted bias in-place dx")
+    assert_bitwise(dbi, db, "weighted bias in-place dbias")
+    assert_bitwise(dwi, dw, "weighted bias in-place dw")
+    # the two reductions are deterministic: a second call gives the same bits
+    dx2, db2, dw2 = sw.swiglu_gateup_weighted_bias_bwd(dyd, xd, bd, wd)
+    torch.cuda.synchronize()
+    assert_bitwise(db2, db, "weighted bias dbias, second call")
+    assert_bitwise(dw2, dw, "weighted bias dw, second call")
+    # with unit weights the combined form is the bias form
+    ones = torch.ones(r, device="cuda")
+    assert_bitwise(sw.swiglu_gateup_weighted_bias_fwd(xd, bd, ones), sw.swiglu_gateup_bias_fwd(xd, bd),
+                   "unit weights fwd")
+    dx1, db1, _ = sw.swiglu_gateup_weighted_bias_bwd(dyd, xd, bd, ones)
+    dxb, dbb = sw.swiglu_gateup_bias_bwd(dyd, xd, bd)
+    torch.cuda.synchronize()
+    assert_bitwise(dx1, dxb, "unit weights dx")
+    assert_bitwise(db1, dbb, "unit weights dbias")
+
+
+def test_weighted_bias_full_size(sw):
+    """Large-FFN workload at full size: y, dx and dw on sampled rows, dbias on
+    sampled columns (the oracle over all 8192 rows of those columns)."""
+    w_ = W.WORKLOADS["large_32768_bf16"]
+    x, dy = W.make_inputs(w_, "cuda")
+    n = w_.n
+    g = torch.Generator().manual_seed(10)
+    bias = (torch.randn(2 * n, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    wts = torch.rand(w_.rows, generator=g).cuda()
+    dx, db, dw = sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts)
+    y = sw.swiglu_gateup_weighted_bias_fwd(x, bias, wts)
+    torch.cuda.synchronize()
+    idx = torch.tensor([0, 1, 4097, 8190, 8191], device="cuda")
+    xs, dys, ws, bc = x[idx].cpu(), dy[idx].cpu(), wts[idx].cpu(), bias.cpu()
+    assert_parity(y[idx], oracle.weighted_bias_fwd(xs, bc, ws), "full weighted bias fwd rows")
+    assert_parity(dx[idx], oracle.weighted_bias_bwd(dys, xs, bc, ws)[0], "full weighted bias dx rows")
+    t = dys.double() * oracle.bias_fwd(xs.double(), bc.double())
+    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "full dw rows")
+    cols = torch.tensor(sorted(set([0, 1, 2047, 2048, n - 1] +
+                                   torch.randperm(n, generator=g)[:59].tolist())))
+    cc = cols.cuda()
+    xsub = torch.cat([x[:, cc], x[:, n + cc]], 1).cpu()
+    dysub = dy[:, cc].cpu()
+    bsub = torch.cat([bias[cc], bias[n + cc]]).cpu()
+    dx64, db64, _ = oracle.weighted_bias_bwd(dysub.double(), xsub.double(), bsub.double(), wts.cpu())
+    got = torch.cat([db[cc], db[n + cc]])
+    assert_reduction(got, db64, dx64.abs().sum(0), _bias_depth(w_.rows, n), "full dbias columns")
+
+
 def test_bias_full_size_columns(sw):
     """Large-FFN workload at full size, the launch configuration of the bench:
     dx on sampled rows, dbias on sampled columns (the oracle over all 8192 rows
@@ -178,6 +261,25 @@ def test_empty_and_workspace_errors(sw):
     sw.swiglu_gateup_weighted_bwd(torch.empty(32, 0, device="cuda"), torch.empty(32, 0, device="cuda"),
                                   torch.ones(32, device="cuda"), dw=dw)
     assert torch.equal(dw, torch.zeros_like(dw))
+    # weights and bias together: no rows zero dbias, no columns zero dw
+    dbias.fill_(7.0)
+    sw.swiglu_gateup_weighted_bias_bwd(torch.empty(0, n, device="cuda"),
+                                       torch.empty(0, 2 * n, device="cuda"), bias,
+                                       torch.empty(0, device="cuda"), dbias=dbias)
+    assert torch.equal(dbias, torch.zeros_like(dbias))
+    dw.fill_(3.0)
+    sw.swiglu_gateup_weighted_bias_bwd(torch.empty(32, 0, device="cuda"),
+                                       torch.empty(32, 0, device="cuda"),
+                                       torch.empty(0, device="cuda"), torch.ones(32, device="cuda"),
+                                       dw=dw)
+    assert torch.equal(dw, torch.zeros_like(dw))
+    need_wb = sw.weighted_bias_bwd_workspace_bytes(32, n)
+    assert need_wb >= need + 32 * 4
+    with pytest.raises(sw.SwigluError) as e:
+        sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, torch.ones(32, device="cuda"),
+                                           workspace=torch.empty(need_wb - 16, dtype=torch.uint8,
+                                                                 device="cuda"))
+    assert e.value.status == -7
 
 
 LAYOUTS = [
@@ -236,6 +338,14 @@ def test_bias_and_weighted_layouts(sw, case):
     assert_parity(yw, oracle.weighted_fwd(x_c, w_c), "weighted fwd")
     t = dy_c.double() * oracle.fwd(x_c.double())
     assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, "weighted dw")
+    dx.fill_(-7.0)
+    assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                       dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"
+    # weights and bias together, into the same guarded dx
+    _, dbw, dww = sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts, dx)
+    ywb = sw.swiglu_gateup_weighted_bias_fwd(x, bias, wts)
+    torch.cuda.synchronize()
+    _check_weighted_bias(dy_c, x_c, bias_c, w_c, ywb, dx, dbw, dww, "weighted bias")
     dx.fill_(-7.0)
     assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
                        dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"

@@ -55,3 +55,33 @@ def test_shape_and_dtype_validation(mod):
         m(torch.zeros(4, 7))
     with pytest.raises(ValueError, match="dtype"):
         m(torch.zeros(4, 8, dtype=torch.float16))
+
+
+def test_native_bias_skips_the_fallback(mod):
+    def fallback(*a):
+        raise AssertionError("fallback must not be called with native_bias=True")
+
+    m = mod(fallback_impl=fallback, native_bias=True)
+    with pytest.raises(ValueError, match="even"):  # validated, then the kernels would run
+        m(torch.zeros(4, 7), torch.zeros(7))
+
+
+def test_weighted_module_policy(caplog):
+    from conftest import build_library
+
+    build_library()
+    from gate_up_swiglu_gb300.autograd import WeightedGateUpSwiGLU
+
+    with pytest.raises(NotImplementedError, match="fp8_input_store"):
+        WeightedGateUpSwiGLU()(torch.zeros(4, 8), None, torch.ones(4), True)
+    calls = []
+    m = WeightedGateUpSwiGLU(fallback_impl=lambda *a: calls.append(a) or "fb")
+    with caplog.at_level(logging.WARNING):
+        assert m(torch.zeros(4, 8), None, torch.ones(4), True) == "fb"
+        assert m(torch.zeros(4, 8), None, torch.ones(4), True) == "fb"
+    assert len(calls) == 2
+    assert sum("fp8_input_store" in r.getMessage() for r in caplog.records) == 1
+    with pytest.raises(ValueError, match="even"):
+        m(torch.zeros(4, 7), None, torch.ones(4))
+    with pytest.raises(ValueError, match="dtype"):
+        m(torch.zeros(4, 8, dtype=torch.float16), None, torch.ones(4))
