@@ -267,3 +267,66 @@ def test_side_stream(sw):
     s.synchronize()
     assert_bitwise(dx, ref, "side stream")
     assert_bitwise(y, sw.swiglu_gateup_fwd(x), "side stream fwd")
+
+
+# ----------------------------------------------------------- maximum sizes ---
+
+def _cols(x, J, n):
+    return torch.cat([x[:, J], x[:, n + J]], 1)
+
+
+def test_maximum_n(sw):
+    """n = 2^30 (the largest the ABI accepts), 2 rows of bf16: element offsets
+    past 2^31 within a row, and the last packs of each half.  Checked on
+    sampled columns (the op is elementwise, so a column subset is a smaller
+    problem of its own)."""
+    n, rows = 1 << 30, 2
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = torch.randn(rows, 2 * n, device="cuda", generator=g, dtype=torch.bfloat16)
+    dy = torch.randn(rows, n, device="cuda", generator=g, dtype=torch.bfloat16)
+    y = sw.swiglu_gateup_fwd(x)
+    dx = sw.swiglu_gateup_bwd(dy, x)
+    torch.cuda.synchronize()
+    J = torch.cat([torch.arange(0, 64), torch.arange((1 << 29) - 32, (1 << 29) + 32),
+                   torch.arange(n - 64, n)]).cuda()
+    xs, dys = _cols(x, J, n).cpu(), dy[:, J].cpu()
+    assert_parity(y[:, J], oracle.fwd(xs), "max n fwd")
+    assert_parity(_cols(dx, J, n), oracle.bwd(dys, xs), "max n bwd")
+    del x, dy, y, dx
+    torch.cuda.empty_cache()
+
+
+def test_more_than_2_32_elements(sw):
+    """2^20 + 3 rows of n = 4104 (4.3e9 gate/up pairs, 8-byte-aligned packs):
+    the flattened (row, pack) index and its carry run past 2^32 in the plain,
+    bias and weights + bias kernels.  Checked on sampled rows, and dbias on
+    sampled columns over all rows."""
+    from test_bias_weighted_gpu import _bias_depth, _wb_dw_depth, assert_reduction
+
+    rows, n = (1 << 20) + 3, 4104
+    g = torch.Generator(device="cuda").manual_seed(13)
+    x = torch.randn(rows, 2 * n, device="cuda", generator=g, dtype=torch.bfloat16)
+    dy = torch.randn(rows, n, device="cuda", generator=g, dtype=torch.bfloat16)
+    bias = (torch.randn(2 * n, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    wts = torch.rand(rows, device="cuda", generator=g)
+    R = torch.tensor([0, 1, 777, (1 << 19) + 5, rows - 2, rows - 1], device="cuda")
+    xs, dys, bc, ws = x[R].cpu(), dy[R].cpu(), bias.cpu(), wts[R].cpu()
+
+    y = sw.swiglu_gateup_fwd(x)
+    assert_parity(y[R], oracle.fwd(xs), "2^32 fwd")
+    del y
+    dx = sw.swiglu_gateup_bwd(dy, x)
+    assert_parity(dx[R], oracle.bwd(dys, xs), "2^32 bwd")
+    dx, db, dw = sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts, dx=dx)
+    torch.cuda.synchronize()
+    assert_parity(dx[R], oracle.weighted_bias_bwd(dys, xs, bc, ws)[0], "2^32 weighted bias dx")
+    t = dys.double() * oracle.bias_fwd(xs.double(), bc.double())
+    assert_reduction(dw[R], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "2^32 dw rows")
+    J = torch.tensor([0, 1, 2047, 2048, 4095, 4096, n - 1], device="cuda")
+    xsub, dysub = _cols(x, J, n).cpu(), dy[:, J].cpu()
+    bsub = torch.cat([bias[J], bias[n + J]]).cpu()
+    dx64, db64, _ = oracle.weighted_bias_bwd(dysub.double(), xsub.double(), bsub.double(), wts.cpu())
+    assert_reduction(torch.cat([db[J], db[n + J]]), db64, dx64.abs().sum(0), _bias_depth(rows, n),
+                     "2^32 dbias columns")
+    del x, dy, dx
+    torch.cuda.empty_cache()
