@@ -30,6 +30,10 @@
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and runs
  *     asynchronously; the call returns after the launch.  The current CUDA
  *     device must be the one that owns the pointers.
+ *   - No call synchronises, allocates or waits on the host, so every entry
+ *     point can be captured into a CUDA graph (stream capture) and replayed;
+ *     the first call on a device caches a few device attributes, which is
+ *     best done once eagerly before capturing.
  *   - Every argument is checked on the host before anything is launched; on
  *     any error nothing is written and nothing is launched.  rows == 0 or
  *     n == 0 is a valid empty call (returns SWIGLU_OK, touches nothing, and
