@@ -124,16 +124,37 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def stored_traffic(kernel_key: str, workload: str):
+def _stored(kernel_key: str, workload: str):
     try:
         with open(TRAFFIC_FILE) as f:
-            d = json.load(f)
-        e = d[kernel_key]
+            e = json.load(f)[kernel_key]
     except (OSError, KeyError, ValueError):
         return None
     if e.get("source_digest") != source_digest() or e.get("workload") != workload:
         return None
-    return e.get("bytes_per_launch")
+    return e
+
+
+def stored_traffic(kernel_key: str, workload: str):
+    e = _stored(kernel_key, workload)
+    return None if e is None else e.get("bytes_per_launch")
+
+
+def ncu_fractions(w) -> dict:
+    """Algorithmic bytes over the ncu-measured kernel durations stored with
+    the traffic capture (mean over its launches), as fractions of 8000 GB/s:
+    the 'as measured by ncu' reading of the HBM target. None when the stored
+    capture is for other sources or another workload."""
+    f, b = _stored("fwd", w.name), _stored("bwd", w.name)
+    if f is None or b is None or not f.get("duration_ns") or not b.get("duration_ns"):
+        return None
+    tf = statistics.mean(f["duration_ns"]) * 1e-9
+    tb = statistics.mean(b["duration_ns"]) * 1e-9
+    fb, bb = w.fwd_bytes(), w.bwd_bytes()
+    return {"fwd": round(fb / tf / 8e12, 4), "bwd": round(bb / tb / 8e12, 4),
+            "fwdbwd": round((fb + bb) / (tf + tb) / 8e12, 4),
+            "fwd_us": round(tf * 1e6, 1), "bwd_us": round(tb * 1e6, 1),
+            "source": "profiles/traffic.json (gpu__time_duration.sum of the same capture)"}
 
 
 def record_traffic(csv_path: str, workload: str = W.HEADLINE) -> dict:
@@ -435,6 +456,7 @@ def ours_arm(args, w):
                                  "peak_gbs": peak, "peak_source": peak_src},
         "frac_of_8000_gbs": {"fwd": round(gbs(fb, fwd_avg) / 8000, 4),
                              "fwdbwd": round(gbs(fb + bb, fwd_avg + bwd_avg) / 8000, 4)},
+        "ncu_frac_of_8000_gbs": ncu_fractions(w),
         "roofline": {"bound": "hbm", "kernel": "swiglu_bwd_kernel (out of place)",
                      "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(bwd_gbs / peak, 4), "peak_source": peak_src,
