@@ -417,6 +417,11 @@ def ours_arm(args, w):
     ip_avg = max_over_ranks(statistics.mean(ip_ms))
 
     extras = measure_extras(sw, w, x, dy, dev, stream, reps=min(K, 100))
+    un = extras.get("unfused_torch_eager")
+    if un:
+        # the page's headline is the fused kernel's gain over the unfused path
+        un["fused_speedup_fwd"] = round(un["fwd_ms"] / fwd_avg, 3)
+        un["fused_speedup_fwdbwd"] = round((un["fwd_ms"] + un["bwd_ms"]) / (fwd_avg + bwd_avg), 3)
 
     e2e = None
     if not args.no_e2e:
@@ -512,6 +517,22 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
     ag_ms = _event_ms(ag_step, stream, reps)
     del xs
 
+    # the unfused path the fused kernel replaces: the same math composed from
+    # eager PyTorch ops on the [rows, 2n] buffer (chunk into halves, silu and
+    # multiply; the backward's two formulas, then a cat), in the storage dtype
+    def unfused_fwd():
+        g_, u_ = x.chunk(2, -1)
+        return torch.nn.functional.silu(g_) * u_
+
+    def unfused_bwd():
+        g_, u_ = x.chunk(2, -1)
+        s_ = torch.sigmoid(g_)
+        return torch.cat((dy * u_ * s_ * (1 + g_ * (1 - s_)), dy * g_ * s_), -1)
+
+    with torch.cuda.stream(stream):
+        uf_ms = _event_ms(unfused_fwd, stream, max(3, min(reps, 20)))
+        ub_ms = _event_ms(unfused_bwd, stream, max(3, min(reps, 20)))
+
     # per-token weights and bias on the same x / dy
     g = torch.Generator().manual_seed(11)
     wts = torch.rand(w.rows, generator=g).to(dev)
@@ -548,6 +569,10 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
     per_workload = measure_workloads(sw, dev, stream, skip=w.name, reps=max(5, min(reps, 50)))
 
     return {
+        "unfused_torch_eager": {
+            "what": "eager PyTorch ops on the same buffers: fwd chunk + silu * up, bwd chunk + "
+                    "the two formulas + cat (intermediates rounded to the storage dtype)",
+            "fwd_ms": round(uf_ms, 4), "bwd_ms": round(ub_ms, 4)},
         "other_workloads": per_workload,
         "fc1_swiglu_tcgen05": fc1,
         "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "

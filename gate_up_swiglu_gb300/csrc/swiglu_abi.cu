@@ -72,24 +72,36 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
     return 1;
 }
 
-// Launch policy, chosen by sweeping pack width, unroll and resident CTAs per
-// SM on a GB300.  Over the Megatron-shape, large-FFN and Llama-like bf16
-// workloads the forward is fastest with one 32-byte pack per operand in flight
-// and 4 CTAs of 256 threads per SM, both backward forms with two 16-byte packs
-// and 3 CTAs per SM (filling the SM with more CTAs lost 5-10 %).  Narrow packs
-// (4 bytes or less: odd n, misaligned rows) want more threads instead: four
-// packs in flight and 8 (forward) / 6 (backward) CTAs per SM, 6-8 % faster than
-// eight packs at 4 / 3 CTAs on the odd-width fp32 workload.
+// Launch policy, chosen by sweeping pack width, unroll, resident CTAs per SM
+// and grid size on a GB300 (back-to-back launches timed by CUDA events).
+// Forward: with one 32-byte pack per operand and thread, a one-pass grid (a
+// CTA per 256 packs, launched in order) beats every persistent grid -- large
+// FFN 225.6 us against 238.5 us at 4 CTAs per SM, Llama-like 101.9 against
+// 105.5, Megatron shape 31.9 against 34.0: CTAs that start in address order
+// keep the DRAM access window compact, where persistent CTAs drift apart.
+// With 16-byte packs (two in flight) 6 CTAs per SM did best.  The forward
+// variants with a bias or row weights keep persistent grids of 4 CTAs per SM:
+// on the one-pass grid they ran 3-11 % slower.  Backward (both
+// forms): two 16-byte packs in flight and 3 CTAs per SM beat the one-pass grid
+// by 1-2 % on every workload.  Narrow packs (4 bytes or less: odd n,
+// misaligned rows) want more threads: four packs in flight and 8 (forward) /
+// 6 (backward) CTAs per SM.
 struct Policy {
     int max_pack_bytes;
-    int max_ctas_per_sm;
-    int max_ctas_per_sm_narrow;  // packs of 4 bytes or less
+    int ctas_wide;    // 32-byte packs; 0 = a one-pass grid
+    int ctas_medium;  // 8- and 16-byte packs
+    int ctas_narrow;  // packs of 4 bytes or less
 };
-constexpr Policy kFwdPolicy = {32, 4, 8};
-constexpr Policy kBwdPolicy = {16, 3, 6};
+constexpr Policy kFwdPolicy = {32, 0, 6, 8};
+constexpr Policy kFwdModePolicy = {32, 4, 4, 8};  // bias and / or row weights
+constexpr Policy kBwdPolicy = {16, 3, 3, 6};
+// The bias tile kernel is launched as one wave of this many CTAs per SM (its
+// __launch_bounds__ minimum); the workspace size follows from it.
+constexpr int kBiasCtasPerSm = 3;
 
+// Resident CTAs per SM to launch with, 0 for a one-pass grid.
 constexpr int ctas_cap(const Policy &p, int pack_bytes) {
-    return pack_bytes <= 4 ? p.max_ctas_per_sm_narrow : p.max_ctas_per_sm;
+    return pack_bytes >= 32 ? p.ctas_wide : (pack_bytes > 4 ? p.ctas_medium : p.ctas_narrow);
 }
 
 // Packs in flight per operand per thread: one 32-byte pack, two 16-byte
@@ -148,7 +160,9 @@ template <int U>
 int64_t grid_for(int64_t total_packs, const Device &d, int per_sm) {
     const int64_t per_cta = (int64_t)U * swiglu::kThreads;
     int64_t need = (total_packs + per_cta - 1) / per_cta;
-    int64_t full = (int64_t)d.sms * per_sm;
+    // per_sm == 0: one pass (bounded by the launch limit; the kernels' grid
+    // stride covers anything beyond it)
+    int64_t full = per_sm > 0 ? (int64_t)d.sms * per_sm : (int64_t)INT32_MAX;
     return need < full ? need : full;
 }
 
@@ -179,7 +193,8 @@ struct BwdArgs {
 };
 
 // Row groups of the bias backward: enough (column tile, row group) CTAs to
-// fill every SM with kBwdPolicy.max_ctas_per_sm of them, once.
+// fill every SM with kBiasCtasPerSm of them (the tile kernel's launch bound),
+// once.
 struct BiasPlan {
     int64_t tiles, groups, rows_per_group;
     size_t workspace_bytes;
@@ -188,7 +203,7 @@ struct BiasPlan {
 BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {  // rows, n >= 1
     BiasPlan b;
     b.tiles = (n + swiglu::kBiasTileCols - 1) / swiglu::kBiasTileCols;
-    int64_t groups = ((int64_t)sms * kBwdPolicy.max_ctas_per_sm) / b.tiles;
+    int64_t groups = ((int64_t)sms * kBiasCtasPerSm) / b.tiles;
     if (groups < 1) groups = 1;
     if (groups > rows) groups = rows;
     b.rows_per_group = (rows + groups - 1) / groups;
@@ -218,9 +233,12 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
-    e = ctas_per_sm(kernel, d, occ, per_sm);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (per_sm > ctas_cap(kFwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kFwdPolicy, E::kBytes * VEC);
+    constexpr int cap = ctas_cap(MODE == swiglu::kPlain ? kFwdPolicy : kFwdModePolicy, E::kBytes * VEC);
+    if (cap > 0) {
+        e = ctas_per_sm(kernel, d, occ, per_sm);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (per_sm > cap) per_sm = cap;
+    }
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -280,6 +298,7 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
+    static_assert(ctas_cap(kBwdPolicy, E::kBytes * VEC) > 0, "backward grids are persistent");
     if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
@@ -305,6 +324,7 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
+    static_assert(ctas_cap(kBwdPolicy, E::kBytes * VEC) > 0, "backward grids are persistent");
     if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     int64_t grid = (int64_t)d.sms * per_sm;
     if (grid > a.rows) grid = a.rows;
