@@ -81,11 +81,13 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 // keep the DRAM access window compact, where persistent CTAs drift apart.
 // With 16-byte packs (two in flight) 6 CTAs per SM did best.  The forward
 // variants with a bias or row weights keep persistent grids of 4 CTAs per SM:
-// on the one-pass grid they ran 3-11 % slower.  Backward (both
-// forms): two 16-byte packs in flight and 3 CTAs per SM beat the one-pass grid
-// by 1-2 % on every workload.  Narrow packs (4 bytes or less: odd n,
-// misaligned rows) want more threads: four packs in flight and 8 (forward) /
-// 6 (backward) CTAs per SM.
+// on the one-pass grid they ran 3-11 % slower.  Backward (both forms), two
+// 16-byte packs in flight: once the pack-level deep-tail test took ~5
+// instructions per element out of the common path, the one-pass grid won as
+// well -- large FFN 386.0 us against 399-418 us at 3 CTAs per SM, Llama-like
+// 172.2 against 177.6, in place 389.2 against 403.5.  Narrow packs (4 bytes
+// or less: odd n, misaligned rows) want persistent CTAs with more threads:
+// four packs in flight and 8 (forward) / 6 (backward) CTAs per SM.
 struct Policy {
     int max_pack_bytes;
     int ctas_wide;    // 32-byte packs; 0 = a one-pass grid
@@ -94,7 +96,9 @@ struct Policy {
 };
 constexpr Policy kFwdPolicy = {32, 0, 6, 8};
 constexpr Policy kFwdModePolicy = {32, 4, 4, 8};  // bias and / or row weights
-constexpr Policy kBwdPolicy = {16, 3, 3, 6};
+constexpr Policy kBwdPolicy = {16, 0, 0, 6};
+// The per-token-weighted backward is one CTA per row, persistent over rows.
+constexpr Policy kRowPolicy = {16, 3, 3, 6};
 // The bias tile kernel is launched as one wave of this many CTAs per SM (its
 // __launch_bounds__ minimum); the workspace size follows from it.
 constexpr int kBiasCtasPerSm = 3;
@@ -296,10 +300,12 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
-    e = ctas_per_sm(kernel, d, occ, per_sm);
-    if (e != cudaSuccess) return cuda_fail(e);
-    static_assert(ctas_cap(kBwdPolicy, E::kBytes * VEC) > 0, "backward grids are persistent");
-    if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
+    constexpr int cap = ctas_cap(kBwdPolicy, E::kBytes * VEC);
+    if (cap > 0) {
+        e = ctas_per_sm(kernel, d, occ, per_sm);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (per_sm > cap) per_sm = cap;
+    }
     const int64_t nvec = a.n / VEC;
     const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
     const int64_t step = grid * U * swiglu::kThreads;
@@ -324,8 +330,8 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     e = ctas_per_sm(kernel, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
-    static_assert(ctas_cap(kBwdPolicy, E::kBytes * VEC) > 0, "backward grids are persistent");
-    if (per_sm > ctas_cap(kBwdPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kBwdPolicy, E::kBytes * VEC);
+    static_assert(ctas_cap(kRowPolicy, E::kBytes * VEC) > 0, "the row kernel is persistent");
+    if (per_sm > ctas_cap(kRowPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kRowPolicy, E::kBytes * VEC);
     int64_t grid = (int64_t)d.sms * per_sm;
     if (grid > a.rows) grid = a.rows;
     kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(bwd_params(a, VEC));

@@ -248,13 +248,15 @@ __device__ __forceinline__ float two_sum(float a, float b, float &e) {
 // g_lo: a correction the exact gate value carries beyond the fp32 g (the
 // rounding error of g + bias); only the root window of silu' is sensitive
 // enough to need it.
-template <typename E, bool kGrad>
+// kMayDeep = false: the caller knows g >= -64 (or NaN), so the deep-tail
+// scaling is left out (scale is exactly 1; same bits as the general form).
+template <typename E, bool kGrad, bool kMayDeep = true>
 __device__ __forceinline__ Act activation(float g, float g_lo = 0.0f) {
     const float a = fabsf(g);
     const bool pos = g >= 0.0f;
     // deep: for g < -64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or
     // without the scaling and r = 1 stays exact
-    const bool deep = E::kDeepScale && g < -64.0f;
+    const bool deep = E::kDeepScale && kMayDeep && g < -64.0f;
     float t;
     if (E::kFastExp) {
         // t = 2^(-|g| log2 e (+ 64 when deep))
@@ -278,6 +280,18 @@ __device__ __forceinline__ Act activation(float g, float g_lo = 0.0f) {
         }
     }
     return o;
+}
+
+// True when some gate of the pack is below -64, where the storage type needs
+// the deep-tail scaling (never for fp32).  NaN gates do not count, as in the
+// scalar test.
+template <typename E, int VEC>
+__device__ __forceinline__ bool pack_has_deep(const uint32_t *g) {
+    if (!E::kDeepScale) return false;
+    float m = E::get(g, 0);
+#pragma unroll
+    for (int i = 1; i < VEC; ++i) m = fminf(m, E::get(g, i));
+    return m < -64.0f;
 }
 
 // Round VEC fp32 results into the words of one pack (pairs at a time when
@@ -426,6 +440,27 @@ __global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_
     }
 }
 
+// The backward of one pack: dgate and dup in fp32.
+template <typename E, int VEC, bool kMayDeep>
+__device__ __forceinline__ void bwd_pack(const uint32_t *d, const uint32_t *g, const uint32_t *u,
+                                         float *gv, float *uv) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const float gf = E::get(g, i);
+        const float uf = E::get(u, i);
+        const float df = E::get(d, i);
+        const Act act = activation<E, true, kMayDeep>(gf);
+        float a = __fmul_rn(df, __fmul_rn(uf, act.dsilu));
+        float b = __fmul_rn(df, act.silu);
+        if (kMayDeep) {
+            a = __fmul_rn(a, act.scale);
+            b = __fmul_rn(b, act.scale);
+        }
+        gv[i] = a;
+        uv[i] = b;
+    }
+}
+
 // IN_PLACE selects nothing but the aliasing contract (an output may be the
 // very buffer of the matching input, so LD must be a coherent kind); the
 // arithmetic is the same template body, so both instances give identical bits.
@@ -461,15 +496,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
             if (r[k] < p.rows) {
                 uint32_t og[NW] = {}, ou[NW] = {};
                 float gv[VEC], uv[VEC];
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    const float gf = E::get(g[k], i);
-                    const float uf = E::get(u[k], i);
-                    const float df = E::get(d[k], i);
-                    const Act act = activation<E, true>(gf);
-                    gv[i] = __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale);
-                    uv[i] = __fmul_rn(__fmul_rn(df, act.silu), act.scale);
-                }
+                if (pack_has_deep<E, VEC>(g[k]))
+                    bwd_pack<E, VEC, true>(d[k], g[k], u[k], gv, uv);
+                else
+                    bwd_pack<E, VEC, false>(d[k], g[k], u[k], gv, uv);
                 store_pack<E, VEC>(og, gv);
                 store_pack<E, VEC>(ou, uv);
                 S::run(dg + (r[k] * p.dg_stride + c[k]) * B, og);
@@ -504,7 +534,7 @@ struct BwdPair {
     float dg, du, dw_term;
 };
 
-template <typename E, int MODE>
+template <typename E, int MODE, bool kMayDeep = true>
 __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float uf, float bgf,
                                                      float buf, float wr) {
     float g_lo = 0.0f;
@@ -515,21 +545,50 @@ __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float u
             gf = __fadd_rn(gf, bgf);
         uf = __fadd_rn(uf, buf);
     }
-    const Act act = activation<E, true>(gf, g_lo);
+    const Act act = activation<E, true, kMayDeep>(gf, g_lo);
     BwdPair<E, MODE> o;
     o.dw_term = 0.0f;
     if (MODE & kWeight) {
         // dw[r] sums dy * silu(g) * u over the row; dy * w drives the gradient
-        o.dw_term = __fmul_rn(__fmul_rn(__fmul_rn(df, act.silu), uf), act.scale);
+        o.dw_term = __fmul_rn(__fmul_rn(df, act.silu), uf);
+        if (kMayDeep) o.dw_term = __fmul_rn(o.dw_term, act.scale);
         df = __fmul_rn(df, wr);
     }
-    o.dg = __fmul_rn(__fmul_rn(df, __fmul_rn(uf, act.dsilu)), act.scale);
-    o.du = __fmul_rn(__fmul_rn(df, act.silu), act.scale);
+    o.dg = __fmul_rn(df, __fmul_rn(uf, act.dsilu));
+    o.du = __fmul_rn(df, act.silu);
+    if (kMayDeep) {
+        o.dg = __fmul_rn(o.dg, act.scale);
+        o.du = __fmul_rn(o.du, act.scale);
+    }
     return o;
+}
+
+// pack_has_deep for the gates shifted by their bias (rounded as bwd_pair
+// rounds them).
+template <typename E, int VEC>
+__device__ __forceinline__ bool pack_has_deep_biased(const uint32_t *g, const uint32_t *bg) {
+    if (!E::kDeepScale) return false;
+    float m = __fadd_rn(E::get(g, 0), E::get(bg, 0));
+#pragma unroll
+    for (int i = 1; i < VEC; ++i) m = fminf(m, __fadd_rn(E::get(g, i), E::get(bg, i)));
+    return m < -64.0f;
 }
 
 // Weighted backward: one CTA per row (persistent over rows), so dw[r] is a
 // fixed-order reduction inside the CTA: no scratch, deterministic.
+template <typename E, int VEC, bool kMayDeep>
+__device__ __forceinline__ void weighted_pack(const uint32_t *d, const uint32_t *g, const uint32_t *u,
+                                              float wr, float &acc, float *gv, float *uv) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const BwdPair<E, kWeight> o = bwd_pair<E, kWeight, kMayDeep>(E::get(d, i), E::get(g, i),
+                                                                     E::get(u, i), 0.0f, 0.0f, wr);
+        acc = __fadd_rn(acc, o.dw_term);
+        gv[i] = o.dg;
+        uv[i] = o.du;
+    }
+}
+
 template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
 __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const BwdParams p) {
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
@@ -563,14 +622,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const Bwd
                 if (c < p.nvec) {
                     uint32_t og[NW] = {}, ou[NW] = {};
                     float gv[VEC], uv[VEC];
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) {
-                        const BwdPair<E, kWeight> o = bwd_pair<E, kWeight>(
-                            E::get(d[k], i), E::get(g[k], i), E::get(u[k], i), 0.0f, 0.0f, wr);
-                        acc = __fadd_rn(acc, o.dw_term);
-                        gv[i] = o.dg;
-                        uv[i] = o.du;
-                    }
+                    if (pack_has_deep<E, VEC>(g[k]))
+                        weighted_pack<E, VEC, true>(d[k], g[k], u[k], wr, acc, gv, uv);
+                    else
+                        weighted_pack<E, VEC, false>(d[k], g[k], u[k], wr, acc, gv, uv);
                     store_pack<E, VEC>(og, gv);
                     store_pack<E, VEC>(ou, uv);
                     S::run(dgr + (int64_t)c * B, og);
@@ -587,6 +642,25 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const Bwd
 // each half for the rows of its row group, writes dx and leaves the column
 // sums of its rows, in fp32, in partial[group][0, 2n).
 constexpr int kBiasTileCols = 2048;
+
+// One pack of the bias backward: dgate / dup into gv / uv, added to the
+// column sums ag / au, and (with weights) the dw terms added to rowsum.
+template <typename E, int VEC, int MODE, bool kMayDeep>
+__device__ __forceinline__ void bias_pack(const uint32_t *d, const uint32_t *g, const uint32_t *u,
+                                          const uint32_t *bg, const uint32_t *bu, float wr,
+                                          float *ag, float *au, float &rowsum, float *gv,
+                                          float *uv) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const BwdPair<E, MODE> o = bwd_pair<E, MODE, kMayDeep>(
+            E::get(d, i), E::get(g, i), E::get(u, i), E::get(bg, i), E::get(bu, i), wr);
+        if (MODE & kWeight) rowsum = __fadd_rn(rowsum, o.dw_term);
+        ag[i] = __fadd_rn(ag[i], o.dg);
+        au[i] = __fadd_rn(au[i], o.du);
+        gv[i] = o.dg;
+        uv[i] = o.du;
+    }
+}
 
 // With WEIGHTED (per-token weights as well), each row's dw terms over the
 // tile's columns are summed across the CTA into partial_dw[row, tile]: every
@@ -655,18 +729,12 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                 if (r < r1 && c[k] < p.nvec) {
                     uint32_t og[NW] = {}, ou[NW] = {};
                     float gv[VEC], uv[VEC];
-#pragma unroll
-                    for (int i = 0; i < VEC; ++i) {
-                        const BwdPair<E, MODE> o =
-                            bwd_pair<E, MODE>(E::get(d[q][k], i), E::get(g[q][k], i),
-                                              E::get(u[q][k], i), E::get(bg[k], i),
-                                              E::get(bu[k], i), wr);
-                        if (WEIGHTED) rowsum = __fadd_rn(rowsum, o.dw_term);
-                        ag[k][i] = __fadd_rn(ag[k][i], o.dg);
-                        au[k][i] = __fadd_rn(au[k][i], o.du);
-                        gv[i] = o.dg;
-                        uv[i] = o.du;
-                    }
+                    if (pack_has_deep_biased<E, VEC>(g[q][k], bg[k]))
+                        bias_pack<E, VEC, MODE, true>(d[q][k], g[q][k], u[q][k], bg[k], bu[k], wr,
+                                                      ag[k], au[k], rowsum, gv, uv);
+                    else
+                        bias_pack<E, VEC, MODE, false>(d[q][k], g[q][k], u[q][k], bg[k], bu[k], wr,
+                                                       ag[k], au[k], rowsum, gv, uv);
                     store_pack<E, VEC>(og, gv);
                     store_pack<E, VEC>(ou, uv);
                     S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
