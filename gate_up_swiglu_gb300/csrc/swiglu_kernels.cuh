@@ -294,6 +294,17 @@ __device__ __forceinline__ bool pack_has_deep(const uint32_t *g) {
     return m < -64.0f;
 }
 
+// pack_has_deep for the gates shifted by their bias (rounded as bwd_pair
+// rounds them).
+template <typename E, int VEC>
+__device__ __forceinline__ bool pack_has_deep_biased(const uint32_t *g, const uint32_t *bg) {
+    if (!E::kDeepScale) return false;
+    float m = __fadd_rn(E::get(g, 0), E::get(bg, 0));
+#pragma unroll
+    for (int i = 1; i < VEC; ++i) m = fminf(m, __fadd_rn(E::get(g, i), E::get(bg, i)));
+    return m < -64.0f;
+}
+
 // Round VEC fp32 results into the words of one pack (pairs at a time when
 // there are pairs).
 template <typename E, int VEC>
@@ -386,6 +397,25 @@ __device__ __forceinline__ void advance(int64_t step_q, int32_t step_r, int32_t 
     }
 }
 
+// One pack of the forward into yv.
+template <typename E, int VEC, int MODE, bool kMayDeep>
+__device__ __forceinline__ void fwd_pack(const uint32_t *g, const uint32_t *u, const uint32_t *bg,
+                                         const uint32_t *bu, float wr, float *yv) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        float gf = E::get(g, i), uf = E::get(u, i);
+        if (MODE & kBias) {
+            gf = __fadd_rn(gf, E::get(bg, i));
+            uf = __fadd_rn(uf, E::get(bu, i));
+        }
+        const Act act = activation<E, false, kMayDeep>(gf);
+        float v = __fmul_rn(act.silu, uf);
+        if (MODE & kWeight) v = __fmul_rn(v, wr);
+        if (kMayDeep) v = __fmul_rn(v, act.scale);
+        yv[i] = v;
+    }
+}
+
 template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain>
 __global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
@@ -405,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_
         float wr[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
+            wr[k] = 1.0f;
             if (r[k] < p.rows) {
                 L::run(gp + (r[k] * p.g_stride + c[k]) * B, g[k]);
                 L::run(up + (r[k] * p.u_stride + c[k]) * B, u[k]);
@@ -420,18 +451,17 @@ __global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_
             if (r[k] < p.rows) {
                 uint32_t o[NW] = {};
                 float yv[VEC];
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) {
-                    float gf = E::get(g[k], i), uf = E::get(u[k], i);
-                    if (MODE & kBias) {
-                        gf = __fadd_rn(gf, E::get(bg[k], i));
-                        uf = __fadd_rn(uf, E::get(bu[k], i));
-                    }
-                    const Act act = activation<E, false>(gf);
-                    float v = __fmul_rn(act.silu, uf);
-                    if (MODE & kWeight) v = __fmul_rn(v, wr[k]);
-                    yv[i] = __fmul_rn(v, act.scale);
-                }
+                // the pack-level split paid for the plain and the weights +
+                // bias forms and cost 5-6 % for bias or weights alone (same
+                // bits either way)
+                constexpr bool kSplit = MODE == kPlain || MODE == kBiasWeight;
+                const bool deep = !kSplit ? true
+                                  : (MODE & kBias) ? pack_has_deep_biased<E, VEC>(g[k], bg[k])
+                                                   : pack_has_deep<E, VEC>(g[k]);
+                if (deep)
+                    fwd_pack<E, VEC, MODE, true>(g[k], u[k], bg[k], bu[k], wr[k], yv);
+                else
+                    fwd_pack<E, VEC, MODE, false>(g[k], u[k], bg[k], bu[k], wr[k], yv);
                 store_pack<E, VEC>(o, yv);
                 S::run(y + (r[k] * p.y_stride + c[k]) * B, o);
             }
@@ -561,17 +591,6 @@ __device__ __forceinline__ BwdPair<E, MODE> bwd_pair(float df, float gf, float u
         o.du = __fmul_rn(o.du, act.scale);
     }
     return o;
-}
-
-// pack_has_deep for the gates shifted by their bias (rounded as bwd_pair
-// rounds them).
-template <typename E, int VEC>
-__device__ __forceinline__ bool pack_has_deep_biased(const uint32_t *g, const uint32_t *bg) {
-    if (!E::kDeepScale) return false;
-    float m = __fadd_rn(E::get(g, 0), E::get(bg, 0));
-#pragma unroll
-    for (int i = 1; i < VEC; ++i) m = fminf(m, __fadd_rn(E::get(g, i), E::get(bg, i)));
-    return m < -64.0f;
 }
 
 // Weighted backward: one CTA per row (persistent over rows), so dw[r] is a
