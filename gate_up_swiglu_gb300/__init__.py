@@ -16,6 +16,7 @@ copy (§Megatron feature compatibility).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -128,10 +129,26 @@ def _rows_view(t: torch.Tensor, name: str):
     return rows, cols, stride
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(t: torch.Tensor, stream) -> int:
+    """The cudaStream_t to launch on: `stream` (a torch stream or a raw
+    handle), else the current stream of t's device."""
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(t.device.index))
         stream = torch.cuda.current_stream(t.device)
     return int(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _on_device(dev):
+    """Make `dev` current for the call (the library launches on the current
+    device); a no-op when it already is, which is the common case and saves
+    the context switch on every call."""
+    if dev.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
 
 
 def _check_cuda(*ts):
@@ -157,7 +174,7 @@ def swiglu_gateup_fwd(x: torch.Tensor, y: torch.Tensor = None, stream=None) -> t
     yrows, n, sy = _rows_view(y, "y")
     if yrows != rows or n * 2 != two_n:
         raise ValueError("y must be [..., n] with the rows of x")
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_fwd(x.data_ptr(), y.data_ptr(), rows, n, sx, sy, _DTYPE[x.dtype],
                                    _stream_handle(x, stream))
     if st != 0:
@@ -182,7 +199,7 @@ def swiglu_gateup_bwd(dy: torch.Tensor, x: torch.Tensor, dx: torch.Tensor = None
     dxrows, dxcols, sdx = _rows_view(dx, "dx")
     if two_n % 2 or dyrows != rows or n * 2 != two_n or dxrows != rows or dxcols != two_n:
         raise ValueError("shapes must be dy [..., n], x [..., 2n], dx [..., 2n] over the same rows")
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_bwd(dy.data_ptr(), x.data_ptr(), dx.data_ptr(), rows, n, sdy, sx, sdx,
                                    _DTYPE[x.dtype], 1 if in_place else 0, _stream_handle(x, stream))
     if st != 0:
@@ -200,7 +217,7 @@ def swiglu_silu_mul_fwd(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor = None
     (rb, nb, sb), (rc, nc, sc) = _rows_view(b, "b"), _rows_view(c, "c")
     if (rb, nb) != (rows, n) or (rc, nc) != (rows, n):
         raise ValueError("a, b and c must have the same [..., n] shape")
-    with torch.cuda.device(a.device):
+    with _on_device(a.device):
         st = lib.swiglu_silu_mul_fwd(a.data_ptr(), b.data_ptr(), c.data_ptr(), rows, n, sa, sb, sc,
                                      _DTYPE[a.dtype], _stream_handle(a, stream))
     if st != 0:
@@ -221,7 +238,7 @@ def swiglu_silu_mul_bwd(dc: torch.Tensor, a: torch.Tensor, b: torch.Tensor, da=N
     rows, n = views[1][0], views[1][1]
     if any((v[0], v[1]) != (rows, n) for v in views):
         raise ValueError("dc, a, b, da and db must have the same [..., n] shape")
-    with torch.cuda.device(a.device):
+    with _on_device(a.device):
         st = lib.swiglu_silu_mul_bwd(dc.data_ptr(), a.data_ptr(), b.data_ptr(), da.data_ptr(),
                                      db.data_ptr(), rows, n, *[v[2] for v in views],
                                      _DTYPE[a.dtype], _stream_handle(a, stream))
@@ -246,7 +263,7 @@ def swiglu_gateup_weighted_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor
     if yrows != rows or 2 * n != two_n:
         raise ValueError("y must be [..., n] with the rows of x")
     _vector(w, "w", rows, torch.float32)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_weighted_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, n, sx,
                                             sy, _DTYPE[x.dtype], _stream_handle(x, stream))
     if st != 0:
@@ -271,7 +288,7 @@ def swiglu_gateup_weighted_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tenso
         raise ValueError("shapes must be dy [..., n], x [..., 2n], dx [..., 2n] over the same rows")
     _vector(w, "w", rows, torch.float32)
     _vector(dw, "dw", rows, torch.float32)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_weighted_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
                                             dw.data_ptr(), rows, n, sdy, sx, sdx, _DTYPE[x.dtype],
                                             1 if in_place else 0, _stream_handle(x, stream))
@@ -291,7 +308,7 @@ def swiglu_gateup_bias_fwd(x: torch.Tensor, bias: torch.Tensor, y: torch.Tensor 
     if yrows != rows or 2 * n != two_n:
         raise ValueError("y must be [..., n] with the rows of x")
     _vector(bias, "bias", two_n, x.dtype)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_bias_fwd(x.data_ptr(), bias.data_ptr(), y.data_ptr(), rows, n, sx, sy,
                                         _DTYPE[x.dtype], _stream_handle(x, stream))
     if st != 0:
@@ -327,7 +344,7 @@ def swiglu_gateup_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: torch.Tensor
         raise ValueError("shapes must be dy [..., n], x [..., 2n], dx [..., 2n] over the same rows")
     _vector(bias, "bias", two_n, x.dtype)
     _vector(dbias, "dbias", two_n, x.dtype)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         if workspace is None:
             workspace = torch.empty(max(16, bias_bwd_workspace_bytes(rows, n)), dtype=torch.uint8,
                                     device=x.device)
@@ -353,7 +370,7 @@ def swiglu_gateup_weighted_bias_fwd(x: torch.Tensor, bias: torch.Tensor, w: torc
         raise ValueError("y must be [..., n] with the rows of x")
     _vector(bias, "bias", two_n, x.dtype)
     _vector(w, "w", rows, torch.float32)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_gateup_weighted_bias_fwd(x.data_ptr(), bias.data_ptr(), w.data_ptr(),
                                                  y.data_ptr(), rows, n, sx, sy, _DTYPE[x.dtype],
                                                  _stream_handle(x, stream))
@@ -396,7 +413,7 @@ def swiglu_gateup_weighted_bias_bwd(dy: torch.Tensor, x: torch.Tensor, bias: tor
     _vector(dbias, "dbias", two_n, x.dtype)
     _vector(w, "w", rows, torch.float32)
     _vector(dw, "dw", rows, torch.float32)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         if workspace is None:
             workspace = torch.empty(max(16, weighted_bias_bwd_workspace_bytes(rows, n)),
                                     dtype=torch.uint8, device=x.device)
@@ -427,7 +444,7 @@ def swiglu_fc1_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor = None,
     _check_cuda(*ts)
     if not all(t.is_contiguous() for t in ts):
         raise ValueError("swiglu_fc1_fwd needs contiguous tensors")
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = lib.swiglu_fc1_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(),
                                 x_out.data_ptr() if x_out is not None else None, M, n, K,
                                 _DTYPE[x.dtype], _stream_handle(x, stream))
