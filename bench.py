@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+    python bench.py --record-traffic NCU_CSV    # store an ncu DRAM capture
 
 One step = one forward plus one out-of-place backward (the "fwd+bwd" of the
 Liger-Kernel Megatron SwiGLU page, §Summary) over the large-FFN bf16 workload
@@ -12,8 +13,12 @@ ONE JSON line on rank 0.
 
 The value is milliseconds per step (lower is better).  Alongside: forward-
 and backward-only times, in-place backward time, achieved HBM GB/s against the
-measured copy bandwidth, an end-to-end time through host buffers, and the
-oracle timed on the host's cores on a bounded sample of the same workload.
+measured copy bandwidth (and, from the stored ncu capture, against 8 TB/s),
+an end-to-end time through host buffers, the oracle timed on the host's cores
+on a bounded sample of the same workload, and under "extras" the other rows
+(two-tensor, per-token weights, bias, both, the autograd module, an unfused
+eager PyTorch composition of the same math, fc1 + SwiGLU on the tensor cores
+against cuBLAS) and the other workloads.
 
 Under torchrun (--gpus N > 1) every rank runs the whole workload on its own GPU
 (independent replicas: the op has no exchange step), time is the max over
