@@ -35,6 +35,7 @@ import csv
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -119,13 +120,22 @@ def measured_peaks():
 STREAMING_SOURCES = ("swiglu_kernels.cuh", "silu_root_poly.h", "swiglu_abi.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed, so that
+    editing a comment does not invalidate stored counters."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_digest() -> str:
-    """Digest of the streaming kernels' sources, to tell whether stored ncu
-    counters still describe the kernels the bench times."""
+    """Digest of the streaming kernels' code (comments and layout ignored), to
+    tell whether stored ncu counters still describe the kernels the bench
+    times."""
     h = hashlib.sha256()
     for name in STREAMING_SOURCES:
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,11 +9,12 @@
 // The work is pure streaming: 3n (forward) or 5n (backward) elements of HBM
 // traffic per row and ~20 fp32 operations per element pair, so the kernels are
 // bound by HBM bandwidth, not by arithmetic; tensor cores have nothing to do
-// here.  Each thread moves aligned VEC-element packs (16 bytes when the shapes,
-// strides and pointers allow it, narrower otherwise, one element for odd n)
-// with streaming cache hints, keeps U independent packs per operand in flight,
-// and a persistent grid (a whole number of resident CTAs on every SM) strides
-// over the flattened (row, pack) index space.
+// here.  Each thread moves aligned VEC-element packs (32 or 16 bytes when the
+// shapes, strides and pointers allow it, narrower otherwise, one element for
+// odd n) with streaming cache hints and keeps U independent packs per operand
+// in flight; the grid strides over the flattened (row, pack) index space,
+// either in one pass (a CTA per U * kThreads packs) or as a persistent grid
+// of a few resident CTAs per SM, as the host's launch policy decides.
 #pragma once
 
 #include <cuda_bf16.h>
