@@ -527,17 +527,20 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     if (!make_map(enc, &tm_x, x_in, M, K) || !make_map(enc, &tm_wg, w, n, K) ||
         !make_map(enc, &tm_wu, w_up, n, K))
         return fail(cudaErrorInvalidValue);
-    static std::atomic<bool> attr_set{false};
-    if (!attr_set.load()) {
-        e = cudaFuncSetAttribute(fc1_swiglu_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
-        if (e != cudaSuccess) return fail(e);
-        attr_set.store(true);
-    }
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
+    // the shared-memory opt-in is a per-device function attribute
+    constexpr int kMaxDevices = 64;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    const bool cached = dev >= 0 && dev < kMaxDevices && attr_set[dev].load();
+    if (!cached) {
+        e = cudaFuncSetAttribute(fc1_swiglu_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
+        if (e != cudaSuccess) return fail(e);
+        if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true);
+    }
     const int64_t tiles = ((M + PAIR_M - 1) / PAIR_M) * ((n + BN - 1) / BN);  // 256 x 128 tiles
     if (tiles > INT32_MAX) return SWIGLU_ERR_SHAPE;
     const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;

@@ -263,7 +263,7 @@ swiglu_status_t swiglu_gateup_bias_bwd_noalloc(const void *dy, const void *x, co
  *                 rows [n, 2n) up), contiguous         (read)
  *   y     [M, n]  bf16, contiguous                     (written)
  *   x_out [M, 2n] bf16, contiguous, or NULL            (written)
- * Requirements: n and K multiples of 8, M, K, 2n below 2^31 (else
+ * Requirements: n and K multiples of 8, K >= 8, M, K, 2n below 2^31 (else
  * SWIGLU_ERR_SHAPE); all pointers 16-byte aligned
  * (else SWIGLU_ERR_STRIDE); outputs overlap no input and each other
  * (SWIGLU_ERR_ALIAS); dtype SWIGLU_BF16 (else SWIGLU_ERR_DTYPE).  M == 0 or
