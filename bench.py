@@ -338,7 +338,7 @@ def reference_arm(args, w):
         "config": {"workload": w.name, "shape": list(w.shape), "ffn_local": w.n,
                    "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd"},
         "cpu_baseline": {"value": round(ms, 3), "unit": "ms", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host_cpus": os.cpu_count(), "sample": sample},
         "e2e": {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -446,6 +446,7 @@ def ours_arm(args, w):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         ms, srows, secs = time_oracle(w, target_s=args.cpu_seconds)
         cpu = {"value": round(ms, 3), "unit": "ms", "cores": 1, "kind": "oracle",
+               "host_cpus": os.cpu_count(),
                "sample": f"{srows} of {w.rows} rows (fwd + bwd, {secs:.1f} s single thread), "
                          "scaled to the full workload"}
 
