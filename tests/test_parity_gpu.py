@@ -330,3 +330,49 @@ def test_more_than_2_32_elements(sw):
                      "2^32 dbias columns")
     del x, dy, dx
     torch.cuda.empty_cache()
+
+
+def test_concurrent_threads_on_separate_streams(sw):
+    """The library keeps only per-device caches (atomics) and no per-call
+    state: four host threads calling it at once (ctypes releases the GIL),
+    each on its own stream and buffers, get bit-identical results to a single
+    thread."""
+    import threading
+
+    w = W.WORKLOADS["megatron_4096_bf16"]
+    inputs = [W.make_inputs(w, "cuda", rows=128 + 64 * i) for i in range(4)]
+    g = torch.Generator(device="cuda").manual_seed(9)
+    biases = [(torch.randn(2 * w.n, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+              for _ in range(4)]
+    ref = []
+    for (x, dy), b in zip(inputs, biases):
+        ref.append((sw.swiglu_gateup_fwd(x), sw.swiglu_gateup_bwd(dy, x),
+                    sw.swiglu_gateup_bias_bwd(dy, x, b)))
+    torch.cuda.synchronize()
+    results, errors = [None] * 4, []
+
+    def work(i):
+        try:
+            x, dy = inputs[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    y = sw.swiglu_gateup_fwd(x, stream=s)
+                    dx = sw.swiglu_gateup_bwd(dy, x, stream=s)
+                    dxb, db = sw.swiglu_gateup_bias_bwd(dy, x, biases[i], stream=s)
+            s.synchronize()
+            results[i] = (y, dx, (dxb, db))
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(4):
+        assert_bitwise(results[i][0], ref[i][0], f"thread {i} fwd")
+        assert_bitwise(results[i][1], ref[i][1], f"thread {i} bwd")
+        assert_bitwise(results[i][2][0], ref[i][2][0], f"thread {i} bias dx")
+        assert_bitwise(results[i][2][1], ref[i][2][1], f"thread {i} dbias")
