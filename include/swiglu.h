@@ -21,8 +21,10 @@
  * per-token-weight variants further down are the page's named follow-ups.
  *
  * Conventions shared by every entry point:
- *   - All pointers are DEVICE pointers owned by the caller.  The library never
- *     allocates, frees or retains memory and keeps no per-call state.
+ *   - All pointers are DEVICE pointers owned by the caller.  No call allocates
+ *     or frees memory, and no state survives a call; the one piece of device
+ *     memory the library itself holds is the fixed scratch array of
+ *     swiglu_gateup_bias_bwd_noalloc (below), part of the loaded module.
  *   - Sizes and row strides are counted in ELEMENTS of the dtype; within a row
  *     elements are contiguous.  Row r of x starts at x + r * x_row_stride.
  *   - All tensors of one call share one dtype.  Arithmetic is fp32; each result
