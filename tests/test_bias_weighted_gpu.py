@@ -14,7 +14,6 @@ With weights and bias together, dw is summed per 2048-column tile (8 terms per
 thread, then the CTA's 5 + 8 levels) and the tiles are added in order:
 D = 21 + number of tiles.
 """
-import math
 
 import pytest
 import torch

@@ -19,9 +19,7 @@ What each pin rests on:
 """
 import math
 import os
-import re
 import shutil
-import subprocess
 import tempfile
 
 import numpy as np

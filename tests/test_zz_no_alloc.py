@@ -12,7 +12,6 @@ the fixed array must be refused without touching the outputs.
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes on its own.
 """
-import ctypes
 
 import pytest
 import torch
