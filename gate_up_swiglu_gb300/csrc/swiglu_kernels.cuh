@@ -725,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
         for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
     }
+    int slot = 0;  // rows of the current dw batch held in wpart
     for (int64_t rb = r0; rb < r1; rb += RU) {
         uint32_t d[RU][PPT][NW], g[RU][PPT][NW], u[RU][PPT][NW];
 #pragma unroll
@@ -762,7 +763,6 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                 }
             }
             if (WEIGHTED && r < r1) {  // r is the same for every thread of the CTA
-                const int slot = (int)((r - r0) % kDwBatch);
                 wpart[slot][threadIdx.x] = rowsum;
                 if (slot == kDwBatch - 1 || r == r1 - 1) {
                     __syncthreads();
@@ -777,7 +777,9 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                         if (lane == 0) p.partial_dw[(r - slot + q) * tiles + tile] = t;
                     }
                     __syncthreads();  // wpart is refilled by the next batch
+                    slot = -1;
                 }
+                ++slot;
             }
         }
     }
