@@ -8,7 +8,7 @@ the built library.
 The library is two translation units (the C ABI with the streaming kernel
 templates it instantiates, and the tensor-core linear_fc1 + SwiGLU kernel),
 compiled in parallel and linked against the static CUDA runtime so the .so depends on
-nothing but the driver.  No fast-math: the kernels choose every approximate
+nothing but the NVIDIA driver (libcuda).  No fast-math: the kernels choose every approximate
 operation explicitly and must keep subnormal results.
 """
 from __future__ import annotations

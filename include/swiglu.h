@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-/* Same type as cudaStream_t / CUstream (a pointer to the driver's stream
+/* Same type as cudaStream_t / CUstream (a pointer to the CUDA driver's stream
  * object), declared here so that this header does not need the CUDA headers. */
 typedef struct CUstream_st *swiglu_stream_t;
 
