@@ -298,3 +298,25 @@ class Fc1SwiGLU(torch.nn.Module):
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return Fc1SwiGLUFunction.apply(x, self.weight, self.in_place)
+
+
+# Function forms with the positional signatures of Megatron's activation
+# entry points, for code that calls (or patches in) a function rather than a
+# module.  A bias goes to the fused bias kernels; fp8 input storage and cpu
+# offload of the input are not supported and raise.
+_plain_module = GateUpSwiGLU(native_bias=True)
+_weighted_module = WeightedGateUpSwiGLU()
+
+
+def bias_swiglu_impl(input: torch.Tensor, bias: Optional[torch.Tensor],
+                     fp8_input_store: bool = False, cpu_offload_input: bool = False) -> torch.Tensor:
+    """silu(input[..., :n] + bias[:n]) * (input[..., n:] + bias[n:]) (bias optional),
+    differentiable, on the fused kernels; 2D or 3D input."""
+    return _plain_module(input, bias, fp8_input_store, cpu_offload_input)
+
+
+def weighted_bias_swiglu_impl(input: torch.Tensor, bias: Optional[torch.Tensor],
+                              weights: torch.Tensor, fp8_input_store: bool = False) -> torch.Tensor:
+    """weights[token] * the SwiGLU above (MoE routed experts), differentiable in
+    input, bias and weights."""
+    return _weighted_module(input, bias, weights, fp8_input_store)

@@ -154,3 +154,18 @@ def test_module_native_bias_and_weighted_module(ag):
                   "weighted module fwd")
     with pytest.raises(NotImplementedError):
         mw(x3, None, wts.cuda(), True)
+
+
+def test_function_forms_match_the_modules(ag):
+    w = W.WORKLOADS["megatron_4096_bf16"]
+    x_cpu, dy_cpu = W.make_inputs(w, "cpu", rows=64)
+    n = w.n
+    b_cpu = (torch.randn(2 * n, generator=torch.Generator().manual_seed(5)) * 0.5).to(torch.bfloat16)
+    wts = torch.rand(64, 1, generator=torch.Generator().manual_seed(6))
+    x3 = x_cpu.cuda().view(16, 4, 2 * n)
+    y = ag.bias_swiglu_impl(x3, b_cpu.cuda())
+    assert_parity(y.view(64, n), oracle.bias_fwd(x_cpu, b_cpu), "bias_swiglu_impl")
+    y0 = ag.bias_swiglu_impl(x3, None)
+    assert_parity(y0.view(64, n), oracle.fwd(x_cpu), "bias_swiglu_impl without bias")
+    yw = ag.weighted_bias_swiglu_impl(x_cpu.cuda(), b_cpu.cuda(), wts.cuda())
+    assert_parity(yw, oracle.weighted_bias_fwd(x_cpu, b_cpu, wts.view(-1)), "weighted_bias_swiglu_impl")

@@ -85,3 +85,20 @@ def test_weighted_module_policy(caplog):
         m(torch.zeros(4, 7), None, torch.ones(4))
     with pytest.raises(ValueError, match="dtype"):
         m(torch.zeros(4, 8, dtype=torch.float16), None, torch.ones(4))
+
+
+def test_function_forms_policy():
+    from conftest import build_library
+
+    build_library()
+    from gate_up_swiglu_gb300.autograd import bias_swiglu_impl, weighted_bias_swiglu_impl
+
+    x = torch.zeros(4, 8)
+    with pytest.raises(NotImplementedError, match="fp8_input_store"):
+        bias_swiglu_impl(x, None, True, False)
+    with pytest.raises(NotImplementedError, match="cpu_offload_input"):
+        bias_swiglu_impl(x, None, False, True)
+    with pytest.raises(NotImplementedError, match="fp8_input_store"):
+        weighted_bias_swiglu_impl(x, None, torch.ones(4), True)
+    with pytest.raises(ValueError, match="even"):
+        bias_swiglu_impl(torch.zeros(4, 7), None)
