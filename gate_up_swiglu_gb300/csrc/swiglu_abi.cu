@@ -96,6 +96,11 @@ struct Policy {
 };
 constexpr Policy kFwdPolicy = {32, 0, 6, 8};
 constexpr Policy kFwdModePolicy = {32, 4, 4, 8};  // bias and / or row weights
+// Forward outputs below this size (the Megatron ffn-4096 shape's 67 MB among
+// them) use 16-byte packs at 6 CTAs per SM: 29.4 us against 33.1 us on the
+// one-pass 32-byte grid; the Llama-like (235 MB) and large-FFN shapes are
+// faster on the one-pass grid.
+constexpr int64_t kFwdSmallBytes = (int64_t)128 << 20;
 constexpr Policy kBwdPolicy = {16, 0, 0, 6};
 // The per-token-weighted backward is one CTA per row, persistent over rows.
 constexpr Policy kRowPolicy = {16, 3, 3, 6};
@@ -390,7 +395,11 @@ swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const int64_t strides[3] = {a.g.stride, a.u.stride, a.y.stride};
     const void *ptrs[5] = {a.g.p, a.u.p, a.y.p, a.bias_g, a.bias_u};
     const int np = (a.mode & swiglu::kBias) ? 5 : 3;
-    const int vec = pick_vec(E::kBytes, kFwdPolicy.max_pack_bytes, a.n, strides, 3, ptrs, np);
+    // below kFwdSmallBytes of output the plain forward does better with 16-byte
+    // packs on a persistent grid than with the one-pass 32-byte grid
+    const bool small = a.mode == swiglu::kPlain && a.rows * a.n * E::kBytes < kFwdSmallBytes;
+    const int vec = pick_vec(E::kBytes, small ? 16 : kFwdPolicy.max_pack_bytes, a.n, strides, 3,
+                             ptrs, np);
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);
     if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd_mode<E, 8>(a, st);
