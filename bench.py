@@ -666,12 +666,12 @@ def measure_fc1(sw, dev, stream, reps):
 
     cublas = _event_ms(two_step, stream, reps)
     gemm_only = _event_ms(lambda: torch.matmul(X, Wt.T, out=fc1), stream, reps)
-    peak = None
+    peak, peak_src = None, "measured"
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             peak = float(json.load(f)["bf16_tflops"])
     except (OSError, KeyError, ValueError):
-        peak = 1900.0
+        peak, peak_src = 1900.0, "fallback"
     tf = lambda ms: flops / (ms * 1e-3) / 1e12  # noqa: E731
     return {"shape": "X [8192, 4096] x W [28672, 4096] bf16 -> y [8192, 14336]", "reps": reps,
             "fused_ms": round(fused, 4), "fused_tflops": round(tf(fused), 1),
@@ -679,7 +679,8 @@ def measure_fc1(sw, dev, stream, reps):
             "fused_with_fc1_out_ms": round(fused_fc1, 4),
             "cublas_gemm_plus_swiglu_ms": round(cublas, 4),
             "cublas_gemm_only_ms": round(gemm_only, 4),
-            "cublas_gemm_tflops": round(tf(gemm_only), 1), "peak_bf16_tflops": peak}
+            "cublas_gemm_tflops": round(tf(gemm_only), 1), "peak_bf16_tflops": peak,
+            "peak_source": peak_src}
 
 
 def l2_note(w: W.Workload) -> str:
