@@ -634,6 +634,25 @@ def measure_workloads(sw, dev, stream, skip, reps):
         bi = _event_ms(lambda: sw.swiglu_gateup_bwd(dy, xi, in_place=True, stream=stream),
                        stream, reps)
         gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+        unfused = None
+        if wl.dtype == W.BF16:
+            # the same math as eager PyTorch ops on the same buffers (the
+            # unfused path), at this shape too
+            def uf():
+                g_, u_ = x.chunk(2, -1)
+                return torch.nn.functional.silu(g_) * u_
+
+            def ub():
+                g_, u_ = x.chunk(2, -1)
+                s_ = torch.sigmoid(g_)
+                return torch.cat((dy * u_ * s_ * (1 + g_ * (1 - s_)), dy * g_ * s_), -1)
+
+            with torch.cuda.stream(stream):
+                uf_ms = _event_ms(uf, stream, max(3, min(reps, 20)))
+                ub_ms = _event_ms(ub, stream, max(3, min(reps, 20)))
+            unfused = {"fwd_ms": round(uf_ms, 4), "bwd_ms": round(ub_ms, 4),
+                       "fused_speedup_fwd": round(uf_ms / f, 3),
+                       "fused_speedup_fwdbwd": round((uf_ms + ub_ms) / (f + b), 3)}
         out[name] = {
             "shape": list(wl.shape), "dtype": wl.dtype, "fwd_ms": round(f, 4), "bwd_ms": round(b, 4),
             "bwd_in_place_ms": round(bi, 4), "fwd_gbs": round(gb(wl.fwd_bytes(), f), 1),
@@ -641,7 +660,8 @@ def measure_workloads(sw, dev, stream, skip, reps):
             "fwd_frac_of_measured": round(gb(wl.fwd_bytes(), f) / peak, 4),
             "bwd_frac_of_measured": round(gb(wl.bwd_bytes(), b) / peak, 4),
             "l2": "inputs exceed L2" if 3 * wl.n * wl.rows * wl.elem_bytes > l2
-                  else "inputs fit in L2 (back-to-back launches: L2-resident)"}
+                  else "inputs fit in L2 (back-to-back launches: L2-resident)",
+            "unfused_torch_eager": unfused}
         del x, dy, y, dx, xi
     return out
 
