@@ -432,11 +432,6 @@ def ours_arm(args, w):
     ip_avg = max_over_ranks(statistics.mean(ip_ms))
 
     extras = measure_extras(sw, w, x, dy, dev, stream, reps=min(K, 100))
-    un = extras.get("unfused_torch_eager")
-    if un:
-        # the page's headline is the fused kernel's gain over the unfused path
-        un["fused_speedup_fwd"] = round(un["fwd_ms"] / fwd_avg, 3)
-        un["fused_speedup_fwdbwd"] = round((un["fwd_ms"] + un["bwd_ms"]) / (fwd_avg + bwd_avg), 3)
 
     e2e = None
     if not args.no_e2e:
@@ -549,6 +544,39 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
         uf_ms = _event_ms(unfused_fwd, stream, max(3, min(reps, 20)))
         ub_ms = _event_ms(unfused_bwd, stream, max(3, min(reps, 20)))
 
+    # the fused kernels timed the same way as the baselines (back-to-back
+    # launches of one kind), for like-for-like ratios
+    y_same = torch.empty((w.rows, n), dtype=x.dtype, device=dev)
+    dx_same = torch.empty_like(x)
+    of_ms = _event_ms(lambda: sw.swiglu_gateup_fwd(x, y_same, stream=stream), stream,
+                      max(3, min(reps, 20)))
+    ob_ms = _event_ms(lambda: sw.swiglu_gateup_bwd(dy, x, dx_same, stream=stream), stream,
+                      max(3, min(reps, 20)))
+    del y_same, dx_same
+
+    def speedups(f_ms, b_ms):
+        return {"fused_fwd_ms": round(of_ms, 4), "fused_bwd_ms": round(ob_ms, 4),
+                "fused_speedup_fwd": round(f_ms / of_ms, 3),
+                "fused_speedup_fwdbwd": round((f_ms + b_ms) / (of_ms + ob_ms), 3)}
+
+    # the same code compiled by torch.compile (one fused Triton kernel per
+    # direction): the closest analogue of a compiler-fused framework path
+    compiled = None
+    try:
+        t_c = time.perf_counter()
+        cfwd, cbwd = torch.compile(unfused_fwd), torch.compile(unfused_bwd)
+        with torch.cuda.stream(stream):
+            cfwd()
+            cbwd()
+            torch.cuda.synchronize(dev)
+            compile_s = time.perf_counter() - t_c
+            cf_ms = _event_ms(cfwd, stream, max(3, min(reps, 20)))
+            cb_ms = _event_ms(cbwd, stream, max(3, min(reps, 20)))
+        compiled = {"fwd_ms": round(cf_ms, 4), "bwd_ms": round(cb_ms, 4),
+                    "compile_s": round(compile_s, 1), **speedups(cf_ms, cb_ms)}
+    except Exception as e:  # a box without a working compiler stack
+        compiled = {"unavailable": f"{type(e).__name__}: {str(e)[:120]}"}
+
     # per-token weights and bias on the same x / dy
     g = torch.Generator().manual_seed(11)
     wts = torch.rand(w.rows, generator=g).to(dev)
@@ -590,7 +618,8 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
         "unfused_torch_eager": {
             "what": "eager PyTorch ops on the same buffers: fwd chunk + silu * up, bwd chunk + "
                     "the two formulas + cat (intermediates rounded to the storage dtype)",
-            "fwd_ms": round(uf_ms, 4), "bwd_ms": round(ub_ms, 4)},
+            "fwd_ms": round(uf_ms, 4), "bwd_ms": round(ub_ms, 4), **speedups(uf_ms, ub_ms)},
+        "torch_compile_same_math": compiled,
         "other_workloads": per_workload,
         "fc1_swiglu_tcgen05": fc1,
         "weighted_per_token": row(wf, wb, "fp32 routing weight per row; bwd also returns dw "
