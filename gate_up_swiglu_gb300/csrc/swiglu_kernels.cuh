@@ -373,12 +373,12 @@ struct BwdParams {
     int32_t step_r;
 };
 
-template <int U>
+template <int U, int T = kThreads>
 __device__ __forceinline__ void first_positions(int64_t nvec, int64_t (&r)[U], int32_t (&c)[U]) {
-    const int64_t base = (int64_t)blockIdx.x * (U * kThreads) + threadIdx.x;
+    const int64_t base = (int64_t)blockIdx.x * (U * T) + threadIdx.x;
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-        const int64_t v = base + (int64_t)k * kThreads;
+        const int64_t v = base + (int64_t)k * T;
         r[k] = v / nvec;
         c[k] = (int32_t)(v - r[k] * nvec);
     }
@@ -417,8 +417,9 @@ __device__ __forceinline__ void fwd_pack(const uint32_t *g, const uint32_t *u, c
     }
 }
 
-template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain>
-__global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
+// T: threads per CTA (kThreads unless the launch policy picks another).
+template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain, int T = kThreads>
+__global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     using L = Ld<B, LD>;
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, MODE == kBiasWeight ? 4 : 0) swiglu_
 
     int64_t r[U];
     int32_t c[U];
-    first_positions<U>(p.nvec, r, c);
+    first_positions<U, T>(p.nvec, r, c);
     while (r[0] < p.rows) {
         uint32_t g[U][NW], u[U][NW];
         uint32_t bg[U][NW], bu[U][NW];
