@@ -9,6 +9,8 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <mutex>
+#include <utility>
 
 #include "abi_internal.h"
 #include "swiglu.h"
@@ -86,8 +88,10 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 // instructions per element out of the common path, the one-pass grid won as
 // well -- large FFN 386.0 us against 399-418 us at 3 CTAs per SM, Llama-like
 // 172.2 against 177.6, in place 389.2 against 403.5.  Narrow packs (4 bytes
-// or less: odd n, misaligned rows) want persistent CTAs with more threads:
-// four packs in flight and 8 (forward) / 6 (backward) CTAs per SM.
+// or less: odd n, misaligned rows) of the plain and two-tensor forms go to the
+// row-segment kernels (SegShape below); for the bias and per-token-weight
+// forms they want persistent CTAs with more threads: four packs in flight and
+// 8 (forward) / 6 (backward) CTAs per SM.
 struct Policy {
     int max_pack_bytes;
     int ctas_wide;    // 32-byte packs; 0 = a one-pass grid
@@ -148,13 +152,15 @@ cudaError_t current_device(Device &d) {
     return cudaSuccess;
 }
 
-// Resident CTAs per SM of `kernel` at kThreads threads, cached per device in
-// the caller-provided table (one table per kernel instantiation).
+// Resident CTAs per SM of `kernel` at `threads` threads per CTA and `smem`
+// bytes of dynamic shared memory, cached per device in the caller-provided
+// table (one table per kernel instantiation and launch shape).
 template <typename K>
-cudaError_t ctas_per_sm(K kernel, const Device &d, std::atomic<int> *cache, int &out) {
+cudaError_t ctas_per_sm(K kernel, int threads, const Device &d, std::atomic<int> *cache, int &out,
+                        size_t smem = 0) {
     int v = (d.id >= 0 && d.id < kMaxDevices) ? cache[d.id].load(std::memory_order_relaxed) : 0;
     if (v == 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, swiglu::kThreads, 0);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, smem);
         if (e != cudaSuccess) return e;
         if (v < 1) v = 1;
         if (d.id >= 0 && d.id < kMaxDevices) cache[d.id].store(v, std::memory_order_relaxed);
@@ -163,7 +169,7 @@ cudaError_t ctas_per_sm(K kernel, const Device &d, std::atomic<int> *cache, int 
     return cudaSuccess;
 }
 
-// Persistent grid: never more CTAs than there are units of U * kThreads packs,
+// Persistent grid: never more CTAs than there are units of U * T packs,
 // never more than fill every SM with resident CTAs.
 template <int U, int T = swiglu::kThreads>
 int64_t grid_for(int64_t total_packs, const Device &d, int per_sm) {
@@ -173,6 +179,16 @@ int64_t grid_for(int64_t total_packs, const Device &d, int per_sm) {
     // stride covers anything beyond it)
     int64_t full = per_sm > 0 ? (int64_t)d.sms * per_sm : (int64_t)INT32_MAX;
     return need < full ? need : full;
+}
+
+// Multiplier and shift of swiglu::fast_div for the divisor d >= 1 (the
+// smallest l with 2^l >= d, m = ceil(2^(63 + l) / d)).
+swiglu::FastDiv make_fast_div(uint64_t d) {
+    if (d <= 1) return {0, -1};
+    int l = 0;
+    while (l < 63 && ((uint64_t)1 << l) < d) ++l;
+    const unsigned __int128 num = (unsigned __int128)1 << (63 + l);
+    return {(uint64_t)((num + d - 1) / d), l - 1};
 }
 
 // One operand of a launch: base pointer and row stride in elements.
@@ -247,7 +263,7 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
     if (cap > 0) {
-        e = ctas_per_sm(kernel, d, occ, per_sm);
+        e = ctas_per_sm(kernel, T, d, occ, per_sm);
         if (e != cudaSuccess) return cuda_fail(e);
         if (per_sm > cap) per_sm = cap;
     }
@@ -266,12 +282,78 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     p.u_stride = a.u.stride / VEC;
     p.y_stride = a.y.stride / VEC;
     p.step_q = step / nvec;
+    p.div_nvec = make_fast_div((uint64_t)nvec);
     p.nvec = (int32_t)nvec;
     p.step_r = (int32_t)(step % nvec);
     kernel<<<(unsigned)grid, T, 0, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
+
+// Row-segment kernels (swiglu_rowseg_kernel) for narrow packs: K columns per
+// thread, T threads per CTA, resident CTAs per SM (0 = a one-pass grid).
+// Swept over K in {2, 4, 8, 16}, T in {128, 256, 512} and grids of 4 / 8
+// CTAs per SM or one pass on the fp32 odd-width workload and a bf16
+// [8192, 2 * 14335] case: one pass with 128-thread CTAs did best -- fp32
+// forward 32.3 us (K = 8; 33.1 at K = 8, T = 256; 34.8 at 8 CTAs per SM),
+// backward 53.3 us (K = 8; 55.3 at T = 256), bf16 forward 135.2 us at K = 16
+// (141.4 at K = 8), backward 219.6 us at K = 8.  The per-element walk these
+// kernels replace took 44.5 / 62.4 us on the fp32 workload.
+template <typename E, int MODE>
+struct SegShape {
+    static constexpr int K = 8, T = 128, per_sm = 0;
+};
+template <>
+struct SegShape<swiglu::BF16, swiglu::kSegFwd> {
+    static constexpr int K = 16, T = 128, per_sm = 0;
+};
+
+// Operands: fwd in = {g, u}, out = {y}; bwd in = {dy, g, u}, out = {dg, du}.
+template <typename E, int MODE, bool IN_PLACE>
+swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t rows, int64_t n,
+                              cudaStream_t stream) {
+    using Sh = SegShape<E, MODE>;
+    constexpr int NIN = MODE == swiglu::kSegFwd ? 2 : 3;
+    constexpr int NOUT = MODE == swiglu::kSegFwd ? 1 : 2;
+    auto kernel = swiglu::swiglu_rowseg_kernel<E, MODE, Sh::K, Sh::T,
+                                               IN_PLACE ? kLoadInPlace : kLoadOutOfPlace>;
+    static std::atomic<int> occ[kMaxDevices];
+    Device d;
+    cudaError_t e = current_device(d);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t chunks = (n + Sh::K * Sh::T - 1) / (Sh::K * Sh::T);
+    const int64_t segments = rows * chunks;
+    int64_t grid = segments;
+    if (Sh::per_sm > 0) {
+        int per_sm = 0;
+        e = ctas_per_sm(kernel, Sh::T, d, occ, per_sm);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (per_sm > Sh::per_sm) per_sm = Sh::per_sm;
+        if (grid > (int64_t)d.sms * per_sm) grid = (int64_t)d.sms * per_sm;
+    }
+    if (grid > INT32_MAX) grid = INT32_MAX;  // the segment loop covers the rest
+    swiglu::SegParams p;
+    for (int x = 0; x < 3; ++x) {
+        p.in[x] = x < NIN ? static_cast<const char *>(in[x].p) : nullptr;
+        p.in_stride[x] = x < NIN ? in[x].stride * E::kBytes : 0;
+    }
+    for (int x = 0; x < 2; ++x) {
+        p.out[x] = x < NOUT ? static_cast<char *>(const_cast<void *>(out[x].p)) : nullptr;
+        p.out_stride[x] = x < NOUT ? out[x].stride * E::kBytes : 0;
+    }
+    p.n = n;
+    p.segments = segments;
+    p.div_chunks = make_fast_div((uint64_t)chunks);
+    p.chunks = (int32_t)chunks;
+    kernel<<<(unsigned)grid, Sh::T, 0, stream>>>(p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+}
+
+// Calls whose operands share no pack wider than this many bytes take the
+// row-segment kernels (plain and two-tensor forms; the bias and
+// per-token-weight forms keep the streaming kernels).
+constexpr int kSegMaxPackBytes = 4;
 
 swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
     swiglu::BwdParams p;
@@ -293,6 +375,7 @@ swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
     p.dg_stride = a.dg.stride / vec;
     p.du_stride = a.du.stride / vec;
     p.nvec = (int32_t)(a.n / vec);
+    p.div_nvec = make_fast_div((uint64_t)(a.n / vec));
     p.step_q = 0;
     p.step_r = 0;
     return p;
@@ -310,7 +393,7 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     int per_sm = 0;
     constexpr int cap = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     if (cap > 0) {
-        e = ctas_per_sm(kernel, d, occ, per_sm);
+        e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, per_sm);
         if (e != cudaSuccess) return cuda_fail(e);
         if (per_sm > cap) per_sm = cap;
     }
@@ -336,7 +419,7 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
-    e = ctas_per_sm(kernel, d, occ, per_sm);
+    e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
     static_assert(ctas_cap(kRowPolicy, E::kBytes * VEC) > 0, "the row kernel is persistent");
     if (per_sm > ctas_cap(kRowPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kRowPolicy, E::kBytes * VEC);
@@ -403,6 +486,10 @@ swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const bool small = a.mode == swiglu::kPlain && a.rows * a.n * E::kBytes < kFwdSmallBytes;
     const int vec = pick_vec(E::kBytes, small ? 16 : kFwdPolicy.max_pack_bytes, a.n, strides, 3,
                              ptrs, np);
+    if (a.mode == swiglu::kPlain && vec * E::kBytes <= kSegMaxPackBytes) {
+        const Operand in[2] = {a.g, a.u};
+        return launch_rowseg<E, swiglu::kSegFwd, false>(in, &a.y, a.rows, a.n, st);
+    }
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);
     if constexpr (kMaxVec >= 8) if (vec == 8) return launch_fwd_mode<E, 8>(a, st);
@@ -417,6 +504,11 @@ swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     const void *ptrs[7] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p, a.bias_g, a.bias_u};
     const int np = (a.mode & swiglu::kBias) ? 7 : 5;
     const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, np);
+    if (a.mode == swiglu::kPlain && vec * E::kBytes <= kSegMaxPackBytes) {
+        const Operand in[3] = {a.dy, a.g, a.u};
+        const Operand out[2] = {a.dg, a.du};
+        return launch_rowseg<E, swiglu::kSegBwd, IP>(in, out, a.rows, a.n, st);
+    }
     constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_bwd<E, 16, IP>(a, st);
     if constexpr (kMaxVec >= 8) if (vec == 8) return launch_bwd<E, 8, IP>(a, st);
@@ -833,17 +925,67 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SWIGLU_NOALLOC_
 
 namespace {
 
-// Device address of g_noalloc_scratch on each device, looked up on the first
-// call made with that device current (host code cannot use the array's name
-// as a device address).
-std::atomic<void *> g_noalloc_addr[kMaxDevices];
+// Device address of g_noalloc_scratch in each CUDA context, looked up on the
+// first call made with that context current (host code cannot use the
+// array's name as a device address).  The cache is keyed on the context's
+// process-unique id, not only on the device: after cudaDeviceReset the
+// device's next primary context loads the module afresh and the array may sit
+// at another address.
+struct NoallocSlot {
+    unsigned long long ctx_id;  // 0: empty
+    void *addr;
+};
+std::mutex g_noalloc_mu;
+NoallocSlot g_noalloc_slot[kMaxDevices];
+
+// The CUDA driver's cuCtxGetCurrent / cuCtxGetId, reached through the
+// runtime's entry-point query (the library links no driver library).
+using CtxGetCurrentFn = int (*)(void **);
+using CtxGetIdFn = int (*)(void *, unsigned long long *);
+
+// Process-unique id of the current context, 0 when there is none or the
+// driver cannot say (then nothing is cached).
+unsigned long long current_context_id() {
+    static const std::pair<CtxGetCurrentFn, CtxGetIdFn> fns = [] {
+        void *cur = nullptr, *id = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess)
+            cur = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q2) !=
+                cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess)
+            id = nullptr;
+        return std::make_pair(reinterpret_cast<CtxGetCurrentFn>(cur),
+                              reinterpret_cast<CtxGetIdFn>(id));
+    }();
+    if (fns.first == nullptr || fns.second == nullptr) return 0;
+    void *ctx = nullptr;
+    unsigned long long id = 0;
+    if (fns.first(&ctx) != 0 || ctx == nullptr) return 0;
+    if (fns.second(ctx, &id) != 0) return 0;
+    return id;
+}
 
 cudaError_t noalloc_scratch(int dev, void **out) {
-    void *p = (dev >= 0 && dev < kMaxDevices) ? g_noalloc_addr[dev].load() : nullptr;
-    if (p == nullptr) {
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) g_noalloc_addr[dev].store(p);
+    const bool cacheable = dev >= 0 && dev < kMaxDevices;
+    if (cacheable) {
+        const unsigned long long id = current_context_id();
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (id != 0 && g_noalloc_slot[dev].ctx_id == id) {
+            *out = g_noalloc_slot[dev].addr;
+            return cudaSuccess;
+        }
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (cacheable) {
+        // the lookup above has made the device's context current
+        const unsigned long long id = current_context_id();
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        g_noalloc_slot[dev] = {id, p};
     }
     *out = p;
     return cudaSuccess;

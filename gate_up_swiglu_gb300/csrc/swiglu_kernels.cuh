@@ -10,11 +10,13 @@
 // traffic per row and ~20 fp32 operations per element pair, so the kernels are
 // bound by HBM bandwidth, not by arithmetic; tensor cores have nothing to do
 // here.  Each thread moves aligned VEC-element packs (32 or 16 bytes when the
-// shapes, strides and pointers allow it, narrower otherwise, one element for
-// odd n) with streaming cache hints and keeps U independent packs per operand
-// in flight; the grid strides over the flattened (row, pack) index space,
-// either in one pass (a CTA per U * kThreads packs) or as a persistent grid
-// of a few resident CTAs per SM, as the host's launch policy decides.
+// shapes, strides and pointers allow it, narrower otherwise) with streaming
+// cache hints and keeps U independent packs per operand in flight; the grid
+// strides over the flattened (row, pack) index space, either in one pass (a
+// CTA per U * T packs, T threads per CTA) or as a persistent grid of a few
+// resident CTAs per SM, as the host's launch policy decides.  Shapes whose
+// operands share no pack wider than 4 bytes (odd n, misaligned rows) go to
+// the row-segment kernels further down.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -318,12 +320,29 @@ __device__ __forceinline__ void store_pack(uint32_t *w, const float *v) {
     }
 }
 
+// ------------------------------------------------ division by an invariant ---
+// v / d for 0 <= v < 2^63 and a divisor d fixed per launch, by one high
+// multiplication and a shift (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994, Theorem 4.2, with N = 63):
+// with l = ceil(log2 d) and m = ceil(2^(63 + l) / d), m < 2^64 and
+// v / d = floor(v m / 2^(63 + l)) = (high 64 bits of v m) >> (l - 1).
+// d == 1 is marked by shift < 0.  The host computes m and the shift.
+struct FastDiv {
+    uint64_t m;
+    int32_t shift;  // l - 1, or -1 when d == 1
+};
+
+__device__ __forceinline__ int64_t fast_div(int64_t v, const FastDiv &f) {
+    return f.shift < 0 ? v : (int64_t)(__umul64hi((uint64_t)v, f.m) >> f.shift);
+}
+
 // ---------------------------------------------------------------- kernels ---
 // The index space is rows x nvec packs per half-row, flattened row-major.
-// Thread t of CTA b starts at pack b * U * kThreads + t + k * kThreads (k < U)
-// and advances by gridDim * U * kThreads packs per iteration; (row, column)
-// of each of its U packs is carried along incrementally (step_q rows plus
-// step_r packs, with one carry), so the loop needs no division.
+// Thread t of CTA b (T threads per CTA) starts at pack b * U * T + t + k * T
+// (k < U) and advances by gridDim * U * T packs per iteration; (row, column)
+// of each of its U packs is found once by a division by the invariant nvec and
+// then carried along incrementally (step_q rows plus step_r packs, with one
+// carry), so the loop itself needs no division.
 // The gate and up operands are addressed separately (base pointer and row
 // stride each), which covers both the fused [rows, 2n] buffer (up = gate + n,
 // same stride) and two separate tensors.
@@ -345,9 +364,10 @@ struct FwdParams {
     int64_t g_stride;  // row strides, in packs
     int64_t u_stride;
     int64_t y_stride;
-    int64_t step_q;    // (gridDim * U * kThreads) / nvec
+    int64_t step_q;    // (gridDim * U * T) / nvec
+    FastDiv div_nvec;  // division by nvec
     int32_t nvec;      // packs per row of each operand (n / VEC)
-    int32_t step_r;    // (gridDim * U * kThreads) % nvec
+    int32_t step_r;    // (gridDim * U * T) % nvec
 };
 
 struct BwdParams {
@@ -369,17 +389,19 @@ struct BwdParams {
     int64_t dg_stride;
     int64_t du_stride;
     int64_t step_q;
+    FastDiv div_nvec;
     int32_t nvec;
     int32_t step_r;
 };
 
 template <int U, int T = kThreads>
-__device__ __forceinline__ void first_positions(int64_t nvec, int64_t (&r)[U], int32_t (&c)[U]) {
+__device__ __forceinline__ void first_positions(int64_t nvec, const FastDiv &div, int64_t (&r)[U],
+                                                int32_t (&c)[U]) {
     const int64_t base = (int64_t)blockIdx.x * (U * T) + threadIdx.x;
 #pragma unroll
     for (int k = 0; k < U; ++k) {
         const int64_t v = base + (int64_t)k * T;
-        r[k] = v / nvec;
+        r[k] = fast_div(v, div);
         c[k] = (int32_t)(v - r[k] * nvec);
     }
 }
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_ker
 
     int64_t r[U];
     int32_t c[U];
-    first_positions<U, T>(p.nvec, r, c);
+    first_positions<U, T>(p.nvec, p.div_nvec, r, c);
     while (r[0] < p.rows) {
         uint32_t g[U][NW], u[U][NW];
         uint32_t bg[U][NW], bu[U][NW];
@@ -496,8 +518,8 @@ __device__ __forceinline__ void bwd_pack(const uint32_t *d, const uint32_t *g, c
 // IN_PLACE selects nothing but the aliasing contract (an output may be the
 // very buffer of the matching input, so LD must be a coherent kind); the
 // arithmetic is the same template body, so both instances give identical bits.
-template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
-__global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p) {
+template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST, int T = kThreads>
+__global__ void __launch_bounds__(T) swiglu_bwd_kernel(const BwdParams p) {
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256),
                   "the in-place backward writes what it reads: no read-only loads");
     constexpr int B = E::kBytes * VEC;
@@ -512,7 +534,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
 
     int64_t r[U];
     int32_t c[U];
-    first_positions<U>(p.nvec, r, c);
+    first_positions<U, T>(p.nvec, p.div_nvec, r, c);
     while (r[0] < p.rows) {
         uint32_t d[U][NW], g[U][NW], u[U][NW];
 #pragma unroll
@@ -539,6 +561,80 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_kernel(const BwdParams p)
             }
         }
         advance<U>(p.step_q, p.step_r, p.nvec, r, c);
+    }
+}
+
+// ----------------------------------------------------- row-segment kernels ---
+// When the operands of a call share no pack wider than 4 bytes -- odd n, or
+// rows and base pointers misaligned to one another, as in the fp32 odd-width
+// workload, where the gate and up of one column sit 12 bytes apart mod 16 and
+// rows 8 bytes apart -- the flattened (row, pack) walk above spends most of
+// its instructions on per-element 64-bit index arithmetic.  These kernels
+// take one segment of K * T columns of one row at a time instead: each thread
+// forms its operand pointers once per segment and reaches its K columns
+// (t, t + T, ..., so a warp touches consecutive elements) through constant
+// offsets, loading all of them before computing any.  The arithmetic is
+// fwd_pack / bwd_pack on one-element packs, so the bits equal those of every
+// other kernel; each column is read and written by one thread, so the
+// in-place backward is the same kernel with coherent loads.
+enum : int { kSegFwd = 0, kSegBwd = 1 };
+
+struct SegParams {
+    const char *in[3];      // fwd: g, u; bwd: dy, g, u (address of row 0, column 0)
+    int64_t in_stride[3];   // row strides in bytes
+    char *out[2];           // fwd: y; bwd: dg, du
+    int64_t out_stride[2];
+    int64_t n;
+    int64_t segments;       // rows * chunks
+    FastDiv div_chunks;     // division by chunks
+    int32_t chunks;         // segments per row: ceil(n / (K * T))
+};
+
+template <typename E, int MODE, int K, int T, int LD>
+__global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
+    constexpr int EB = E::kBytes;
+    constexpr int NIN = MODE == kSegFwd ? 2 : 3;
+    constexpr int NOUT = MODE == kSegFwd ? 1 : 2;
+    for (int64_t seg = blockIdx.x; seg < p.segments; seg += gridDim.x) {
+        const int64_t r = fast_div(seg, p.div_chunks);
+        const int64_t c = (seg - r * p.chunks) * (int64_t)(K * T) + threadIdx.x;
+        // columns of this thread in the segment: c + i * T for i < live
+        const int64_t left = p.n - c;
+        const int live = left <= 0 ? 0 : (left >= (int64_t)(K - 1) * T + 1 ? K : (int)((left + T - 1) / T));
+        const char *ip[NIN];
+#pragma unroll
+        for (int x = 0; x < NIN; ++x) ip[x] = p.in[x] + r * p.in_stride[x] + c * EB;
+        uint32_t w[NIN][K];
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            if (i < live) {
+#pragma unroll
+                for (int x = 0; x < NIN; ++x) Ld<EB, LD>::run(ip[x] + i * T * EB, &w[x][i]);
+            }
+        }
+        char *op[NOUT];
+#pragma unroll
+        for (int x = 0; x < NOUT; ++x) op[x] = p.out[x] + r * p.out_stride[x] + c * EB;
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            if (i < live) {
+                if (MODE == kSegFwd) {
+                    float yv[1];
+                    fwd_pack<E, 1, kPlain, true>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
+                    uint32_t o[1] = {0u};
+                    store_pack<E, 1>(o, yv);
+                    St<EB, kStStream>::run(op[0] + i * T * EB, o);
+                } else {
+                    float gv[1], uv[1];
+                    bwd_pack<E, 1, true>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
+                    uint32_t og[1] = {0u}, ou[1] = {0u};
+                    store_pack<E, 1>(og, gv);
+                    store_pack<E, 1>(ou, uv);
+                    St<EB, kStStream>::run(op[0] + i * T * EB, og);
+                    St<EB, kStStream>::run(op[1] + i * T * EB, ou);
+                }
+            }
+        }
     }
 }
 

@@ -231,12 +231,15 @@ swiglu_status_t swiglu_gateup_weighted_bias_bwd(
  * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - A problem whose scratch need (swiglu_gateup_bias_bwd_workspace_size)
  *     exceeds SWIGLU_NOALLOC_SCRATCH_BYTES is rejected with
- *     SWIGLU_ERR_WORKSPACE before anything is launched.  Need is about
- *     3 * SMs * 2048 * 8 bytes when n is a multiple of 2048 (7 MiB on a 152-SM
- *     GB300), more for ragged n, and 8 n bytes at least.
- *   - The first call on a device looks up the array's device address with
- *     that device current (cudaGetSymbolAddress); make that first call before
- *     any stream capture.
+ *     SWIGLU_ERR_WORKSPACE before anything is launched.  For any rows and n
+ *     the need is at most max(3 * SMs * 2048 * 8, 8 n) bytes, SMs being the
+ *     device's multiprocessor count (7.1 MiB on a 152-SM GB300, so every
+ *     n <= 2^21 fits); it reaches 8 n only when one row group spans the
+ *     whole matrix (n above 3 * SMs * 2048).
+ *   - The first call in a CUDA context (per device, and again after a
+ *     cudaDeviceReset) looks up the array's device address with that device
+ *     current (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
  *   - All calls share the one array, which keeps the last call's contents (the
  *     kernels overwrite every scratch value they later read, so nothing needs
  *     to start at zero).  Calls that overlap on the GPU -- on different streams,
