@@ -50,6 +50,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "SwiGLU gate-up fwd & fwd+bwd ms, HBM GB/s, % of GB300 peak (bf16 S2048 B4)"
+CLOCK_WINDOW_S = 0.6  # shortest span of the clock record around the timed steps
 FALLBACK_HBM_GBS = 6800.0
 CSRC = os.path.join(ROOT, "gate_up_swiglu_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -304,6 +305,23 @@ def time_oracle(w: W.Workload, target_s: float):
 
 # ------------------------------------------------------------------ arms ---
 
+GB300_L2_BYTES = 129 << 20  # used only when no GPU is visible
+
+
+def l2_bytes() -> int:
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return GB300_L2_BYTES
+
+
+def bench_config(w: W.Workload, world: int) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": w.name, "shape": list(w.shape), "ffn_local": w.n,
+            "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd",
+            "parallelism": f"independent replicas x{world}" if world > 1 else "one replica",
+            "l2": l2_note(w)}
+
+
 def reference_arm(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -328,15 +346,17 @@ def reference_arm(args, w):
         oracle.fwd(x, lib=lib)
         oracle.bwd(dy, x, lib=lib)
         times.append(time.perf_counter() - t)
-    ms = statistics.mean(times) / rows * w.rows * 1e3
-    sample = f"{rows} of {w.rows} rows per step, scaled to the full workload; single thread"
+    sample_ms = statistics.mean(times) * 1e3       # what each timed step ran
+    ms = sample_ms / rows * w.rows                  # the full workload, by proportion
+    sample = (f"each step runs fwd + bwd on {rows} of {w.rows} rows ({sample_ms:.1f} ms, "
+              f"single thread); value scales that to all rows")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(ms, 3), "unit": "ms",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms, 3), "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": round(sample_ms, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "shape": list(w.shape), "ffn_local": w.n,
-                   "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd"},
+        "config": bench_config(w, ws),
+        "sample_rows_per_step": rows,
         "cpu_baseline": {"value": round(ms, 3), "unit": "ms", "cores": 1, "kind": "oracle",
                          "host_cpus": os.cpu_count(), "sample": sample},
         "e2e": {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": 0,
@@ -406,14 +426,27 @@ def ours_arm(args, w):
     barrier()
     t_wall1 = time.time()
     launches = 2 * K
+    # the timed steps may be shorter than the clock sampler's period: keep the
+    # same work running, untimed, until the sampled window spans CLOCK_WINDOW_S
+    extra = 0
+    while time.time() - t_wall0 < CLOCK_WINDOW_S:
+        for _ in range(50):
+            fwd()
+            bwd(dx, False)
+        extra += 50
+        torch.cuda.synchronize(dev)
+    t_clk1 = time.time()
     fwd_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     bwd_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     ms_step = max_over_ranks(total_ms / K)
     fwd_avg = max_over_ranks(statistics.mean(fwd_ms))
     bwd_avg = max_over_ranks(statistics.mean(bwd_ms))
-    clk = clocks.summary(t_wall0, t_wall1)
+    clk = clocks.summary(t_wall0, t_clk1)
     clocks.stop()
+    if clk is not None:
+        clk["window_s"] = round(t_clk1 - t_wall0, 3)
+        clk["window_steps"] = f"{K} timed + {extra} untimed steps of the same work"
 
     # in-place backward: x is restored from a copy between launches, outside
     # the events, so each timed launch sees the forward input
@@ -458,10 +491,7 @@ def ours_arm(args, w):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "shape": list(w.shape), "ffn_local": n,
-                   "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": l2_note(w)},
+        "config": bench_config(w, ws),
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
         "bwd_in_place_ms": round(ip_avg, 4),
         "fwd_gbs": round(gbs(fb, fwd_avg), 1), "bwd_gbs": round(bwd_gbs, 1),
@@ -733,7 +763,7 @@ def measure_fc1(sw, dev, stream, reps):
 
 
 def l2_note(w: W.Workload) -> str:
-    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    l2 = l2_bytes()
     inputs = (3 * w.n * w.rows) * w.elem_bytes  # x and dy
     if inputs > l2:
         return (f"no flush: inputs {inputs / 2**20:.0f} MiB > L2 {l2 / 2**20:.0f} MiB; "
@@ -741,14 +771,47 @@ def l2_note(w: W.Workload) -> str:
     return f"inputs {inputs / 2**20:.0f} MiB fit in L2 {l2 / 2**20:.0f} MiB: L2-resident timing"
 
 
+def link_rates(dev, nbytes: int = 1 << 30) -> dict:
+    """Host link rates from pinned memory, same run: one nbytes copy each way
+    alone, then both directions at once on two streams (GB/s, best of 3)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn):
+        ts = []
+        for _ in range(3):
+            torch.cuda.synchronize(dev)
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            ts.append(time.perf_counter() - t)
+        return min(ts)
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    t_in = best(lambda: d_in.copy_(h_in, non_blocking=True))
+    t_out = best(lambda: h_out.copy_(d_out, non_blocking=True))
+    t_both = best(both)
+    return {"h2d_gbs": round(nbytes / t_in / 1e9, 1), "d2h_gbs": round(nbytes / t_out / 1e9, 1),
+            "duplex_each_way_gbs": round(nbytes / t_both / 1e9, 1),
+            "copy_bytes": nbytes, "how": "pinned host memory, host clock, best of 3"}
+
+
 def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
-    """The same step from host memory, through the package's host pipeline
-    (gateup_fwd_bwd_host): the inputs are copied in from pinned host memory and
-    the results copied back, chunk by chunk with copies and kernels overlapped,
-    all inside the timed region (host clock around whole calls, each of which
-    returns once its results are in host memory)."""
-    from gate_up_swiglu_gb300.host_pipeline import (HostPipeline, default_chunk_rows,
-                                                    gateup_fwd_bwd_host)
+    """The same step from host memory, through the C-ABI call
+    swiglu_gateup_fwd_bwd_host: the inputs are copied in from pinned host
+    memory and the results copied back, chunk by chunk with copies and kernels
+    overlapped, all inside the timed region (host clock around whole calls,
+    each of which returns once its results are in host memory).  The staging
+    buffer and streams are set up once, before the timed region."""
+    from gate_up_swiglu_gb300.host_pipeline import HostPipeline, default_chunk_rows
 
     xh = torch.empty(x_dev.shape, dtype=x_dev.dtype, pin_memory=True)
     dyh = torch.empty(dy_dev.shape, dtype=dy_dev.dtype, pin_memory=True)
@@ -757,21 +820,35 @@ def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
     yh = torch.empty((w.rows, w.n), dtype=x_dev.dtype, pin_memory=True)
     dxh = torch.empty(x_dev.shape, dtype=x_dev.dtype, pin_memory=True)
     pipe = HostPipeline(dev, default_chunk_rows(w.n, w.elem_bytes))
+    staging = pipe.staging_for(w.n, x_dev.dtype)
+    streams = (pipe.h2d, pipe.comp, pipe.d2h)
+
+    def step():
+        sw.swiglu_gateup_fwd_bwd_host(xh, dyh, yh, dxh, staging, pipe.chunk_rows, pipe.depth,
+                                      streams)
+
     for _ in range(2):
-        gateup_fwd_bwd_host(xh, dyh, yh, dxh, pipe)
+        step()
     torch.cuda.synchronize(dev)
     barrier()
     t0 = time.perf_counter()
     for _ in range(K):
-        gateup_fwd_bwd_host(xh, dyh, yh, dxh, pipe)
+        step()
     torch.cuda.synchronize(dev)
     barrier()
     ms = reduce((time.perf_counter() - t0) * 1e3 / K)
     h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
     d2h = yh.numel() * yh.element_size() + dxh.numel() * dxh.element_size()
+    del xh, dyh, yh, dxh, staging
+    link = link_rates(dev)
+    # the floor set by the link: the larger direction at the measured duplex rate
+    floor_ms = max(h2d, d2h) / (link["duplex_each_way_gbs"] * 1e9) * 1e3
     return {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
-            "how": f"gateup_fwd_bwd_host, {pipe.chunk_rows}-row chunks, 3 streams"}
+            "how": f"C ABI swiglu_gateup_fwd_bwd_host, {pipe.chunk_rows}-row chunks, "
+                   f"{pipe.depth} staging slots, 3 streams",
+            "host_link": link, "link_floor_ms": round(floor_ms, 3),
+            "frac_of_link_floor": round(floor_ms / ms, 4)}
 
 
 def main():

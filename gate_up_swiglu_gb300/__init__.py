@@ -37,8 +37,10 @@ EXPORTS = ("swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swi
            "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
            "swiglu_gateup_weighted_bias_fwd", "swiglu_gateup_weighted_bias_bwd_workspace_size",
-           "swiglu_gateup_weighted_bias_bwd", "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd", "swiglu_fc1_timeout_flag",
-           "swiglu_status_string", "swiglu_last_cuda_error", "swiglu_abi_version")
+           "swiglu_gateup_weighted_bias_bwd", "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd",
+           "swiglu_fc1_timeout_flag", "swiglu_gateup_fwd_bwd_host_staging_size",
+           "swiglu_gateup_fwd_bwd_host", "swiglu_status_string", "swiglu_last_cuda_error",
+           "swiglu_abi_version")
 
 
 class SwigluError(RuntimeError):
@@ -89,6 +91,12 @@ def _load() -> ctypes.CDLL:
     lib.swiglu_fc1_fwd.restype = i32
     lib.swiglu_fc1_timeout_flag.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.swiglu_fc1_timeout_flag.restype = i32
+    lib.swiglu_gateup_fwd_bwd_host_staging_size.argtypes = [i64, i64, i32, i32,
+                                                            ctypes.POINTER(ctypes.c_size_t)]
+    lib.swiglu_gateup_fwd_bwd_host_staging_size.restype = i32
+    lib.swiglu_gateup_fwd_bwd_host.argtypes = [vp, vp, vp, vp, i64, i64, i32, vp, ctypes.c_size_t,
+                                               i64, i32, vp, vp, vp]
+    lib.swiglu_gateup_fwd_bwd_host.restype = i32
     lib.swiglu_status_string.argtypes = [i32]
     lib.swiglu_status_string.restype = ctypes.c_char_p
     lib.swiglu_last_cuda_error.argtypes = []
@@ -461,9 +469,48 @@ def fc1_timeout_flag() -> int:
     return int(out.value)
 
 
+def host_staging_bytes(chunk_rows: int, n: int, dtype, depth: int) -> int:
+    """Device staging bytes swiglu_gateup_fwd_bwd_host needs for this chunking."""
+    out = ctypes.c_size_t(0)
+    st = lib.swiglu_gateup_fwd_bwd_host_staging_size(int(chunk_rows), int(n), _DTYPE[dtype],
+                                                     int(depth), ctypes.byref(out))
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_fwd_bwd_host_staging_size")
+    return int(out.value)
+
+
+def swiglu_gateup_fwd_bwd_host(x_h: torch.Tensor, dy_h: torch.Tensor, y_h: torch.Tensor,
+                               dx_h: torch.Tensor, staging: torch.Tensor, chunk_rows: int,
+                               depth: int, streams) -> None:
+    """y_h = forward(x_h), dx_h = backward(dy_h, x_h) for contiguous 2D host
+    tensors (pin them for overlap) through the device staging buffer `staging`
+    (a CUDA tensor of at least host_staging_bytes(...) bytes) and the three
+    CUDA streams (h2d, compute, d2h); returns once the results are in y_h and
+    dx_h."""
+    rows, two_n = x_h.shape
+    n = two_n // 2
+    for t, shape in ((x_h, (rows, 2 * n)), (dy_h, (rows, n)), (y_h, (rows, n)), (dx_h, (rows, 2 * n))):
+        if t.device.type != "cpu" or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors x [rows, 2n], "
+                             "dy [rows, n], y [rows, n], dx [rows, 2n]")
+        if t.dtype != x_h.dtype or t.dtype not in _DTYPE:
+            raise ValueError("host buffers must all be float32 or all bfloat16")
+    if not staging.is_cuda:
+        raise ValueError("staging must be a CUDA tensor")
+    h = [int(s.cuda_stream if hasattr(s, "cuda_stream") else s) for s in streams]
+    with _on_device(staging.device):
+        st = lib.swiglu_gateup_fwd_bwd_host(
+            x_h.data_ptr(), dy_h.data_ptr(), y_h.data_ptr(), dx_h.data_ptr(), rows, n,
+            _DTYPE[x_h.dtype], staging.data_ptr(), staging.numel() * staging.element_size(),
+            int(chunk_rows), int(depth), h[0], h[1], h[2])
+    if st != 0:
+        raise SwigluError(st, "swiglu_gateup_fwd_bwd_host")
+
+
 __all__ = ["swiglu_gateup_fwd", "swiglu_gateup_bwd", "swiglu_silu_mul_fwd", "swiglu_silu_mul_bwd",
            "swiglu_gateup_weighted_fwd", "swiglu_gateup_weighted_bwd", "swiglu_gateup_bias_fwd",
            "swiglu_gateup_bias_bwd", "bias_bwd_workspace_bytes", "swiglu_gateup_weighted_bias_fwd",
            "swiglu_gateup_weighted_bias_bwd", "weighted_bias_bwd_workspace_bytes",
-           "swiglu_fc1_fwd", "fc1_timeout_flag", "status_string", "SwigluError", "lib",
+           "swiglu_fc1_fwd", "fc1_timeout_flag", "host_staging_bytes",
+           "swiglu_gateup_fwd_bwd_host", "status_string", "SwigluError", "lib",
            "SWIGLU_F32", "SWIGLU_BF16", "EXPORTS", "LIB_PATH"]

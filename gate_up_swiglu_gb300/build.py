@@ -5,8 +5,9 @@
 Run it as a script (or load it by path): importing the package itself needs
 the built library.
 
-The library is two translation units (the C ABI with the streaming kernel
-templates it instantiates, and the tensor-core linear_fc1 + SwiGLU kernel),
+The library is three translation units (the C ABI with the streaming kernel
+templates it instantiates, the tensor-core linear_fc1 + SwiGLU kernel, and the
+host-buffer pipeline),
 compiled in parallel and linked against the static CUDA runtime so the .so depends on
 nothing but the NVIDIA driver (libcuda).  No fast-math: the kernels choose every approximate
 operation explicitly and must keep subnormal results.
@@ -23,7 +24,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libswiglu.so")
-SOURCES = [os.path.join(CSRC, "swiglu_abi.cu"), os.path.join(CSRC, "fc1_swiglu.cu")]
+SOURCES = [os.path.join(CSRC, "swiglu_abi.cu"), os.path.join(CSRC, "fc1_swiglu.cu"),
+           os.path.join(CSRC, "host_pipeline.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

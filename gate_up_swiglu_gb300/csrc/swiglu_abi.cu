@@ -912,7 +912,7 @@ const char *swiglu_status_string(swiglu_status_t status) {
 
 int swiglu_last_cuda_error(void) { return g_last_cuda_error; }
 
-int swiglu_abi_version(void) { return 4; }
+int swiglu_abi_version(void) { return 5; }
 
 }  // extern "C"
 

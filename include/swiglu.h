@@ -21,7 +21,8 @@
  * per-token-weight variants further down are the page's named follow-ups.
  *
  * Conventions shared by every entry point:
- *   - All pointers are DEVICE pointers owned by the caller.  No call allocates
+ *   - All pointers are DEVICE pointers owned by the caller (the *_host
+ *     arguments of swiglu_gateup_fwd_bwd_host excepted).  No call allocates
  *     or frees memory, and no state survives a call; the one piece of device
  *     memory the library itself holds is the fixed scratch array of
  *     swiglu_gateup_bias_bwd_noalloc (below), part of the loaded module.
@@ -32,10 +33,12 @@
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and runs
  *     asynchronously; the call returns after the launch.  The current CUDA
  *     device must be the one that owns the pointers.
- *   - No call synchronises, allocates or waits on the host, so every entry
- *     point can be captured into a CUDA graph (stream capture) and replayed;
- *     the first call on a device caches a few device attributes, which is
- *     best done once eagerly before capturing.
+ *   - No call synchronises, allocates or waits on the host -- except the
+ *     host-buffer pipeline swiglu_gateup_fwd_bwd_host, which by design returns
+ *     once its results are in host memory -- so every other entry point can
+ *     be captured into a CUDA graph (stream capture) and replayed; the first
+ *     call on a device caches a few device attributes, which is best done once
+ *     eagerly before capturing.
  *   - Every argument is checked on the host before anything is launched; on
  *     any error nothing is written and nothing is launched.  rows == 0 or
  *     n == 0 is a valid empty call (returns SWIGLU_OK, touches nothing, and
@@ -282,6 +285,44 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
 /* *flag = 1 if any swiglu_fc1_fwd launch so far gave up on an internal wait,
  * else 0.  Synchronises with the current device. */
 swiglu_status_t swiglu_fc1_timeout_flag(int *flag);
+
+/*
+ * Forward and backward over HOST buffers, end to end.  The page has no
+ * counterpart (its kernels take device tensors); this serves callers whose fc1
+ * buffer and incoming gradient live in host memory -- offloaded activations,
+ * or tensors kept on the CPU side of the Grace-Blackwell link -- with the same
+ * results as swiglu_gateup_fwd followed by the out-of-place swiglu_gateup_bwd:
+ *   y_host  = forward(x_host),  dx_host = backward(dy_host, x_host)
+ *   x_host  [rows, 2n], dy_host [rows, n]   host memory, read
+ *   y_host  [rows, n],  dx_host [rows, 2n]  host memory, written
+ * All four are contiguous (row strides 2n / n), may overlap none of the others,
+ * and should be page-locked (cudaHostAlloc / cudaHostRegister): pageable
+ * memory gives the same results without the overlap.
+ * Rows go through the device in chunks of chunk_rows (>= 1), `depth` chunks
+ * (1 ... 8) in flight: chunk i is copied in on stream h2d, computed on stream
+ * compute (forward, then the backward in place over the staged x, which is
+ * bit-identical to the out-of-place one) and copied out on stream d2h, so
+ * copies in, kernels and copies out of different chunks overlap.  The three
+ * streams may be the same stream (then nothing overlaps).
+ *   staging  caller-owned DEVICE memory of at least
+ *            swiglu_gateup_fwd_bwd_host_staging_size(chunk_rows, n, dtype,
+ *            depth, &bytes) bytes, 256-byte aligned (else SWIGLU_ERR_WORKSPACE);
+ *            its contents on return are unspecified.
+ * The call allocates no device memory; it creates and destroys 3 * depth CUDA
+ * events, and it blocks until every result is in host memory (it waits on
+ * the three streams), so it cannot be captured into a CUDA graph.  One
+ * memcpy per tensor per chunk; no batched copies.
+ */
+swiglu_status_t swiglu_gateup_fwd_bwd_host_staging_size(int64_t chunk_rows, int64_t n,
+                                                        swiglu_dtype_t dtype, int depth,
+                                                        size_t *bytes);
+
+swiglu_status_t swiglu_gateup_fwd_bwd_host(const void *x_host, const void *dy_host, void *y_host,
+                                           void *dx_host, int64_t rows, int64_t n,
+                                           swiglu_dtype_t dtype, void *staging,
+                                           size_t staging_bytes, int64_t chunk_rows, int depth,
+                                           swiglu_stream_t h2d, swiglu_stream_t compute,
+                                           swiglu_stream_t d2h);
 
 /* Static English text for a status code; never NULL. */
 const char *swiglu_status_string(swiglu_status_t status);

@@ -7,12 +7,15 @@
  *
  * IN_FILE holds x [ROWS, 2N] then dy [ROWS, N], raw, in the element type
  * (DTYPE 0 = fp32, 1 = bf16).  OUT_FILE receives y [ROWS, N], dx [ROWS, 2N]
- * and the in-place dx [ROWS, 2N], raw.  Exit status 0 on success; otherwise
- * the failing call and its status string go to stderr.
+ * and the in-place dx [ROWS, 2N], then y and dx again as computed from
+ * page-locked host buffers by swiglu_gateup_fwd_bwd_host (its own device
+ * staging buffer and three streams), raw.  Exit status 0 on success;
+ * otherwise the failing call and its status string go to stderr.
  */
 #include <cuda_runtime_api.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "swiglu.h"
 
@@ -69,12 +72,42 @@ int main(int argc, char **argv) {
               "swiglu_gateup_bwd in place") ||
         check_cuda(cudaMemcpy(out + by + bx, x, bx, cudaMemcpyDeviceToHost), "copy x"))
         return 1;
+    /* end to end from host memory: chunks of about a third of the rows,
+     * two staging slots, three streams */
+    const int64_t chunk = rows / 3 + 1;
+    const int depth = 2;
+    size_t staging_bytes = 0;
+    void *hx = NULL, *hdy = NULL, *hy = NULL, *hdx = NULL, *staging = NULL;
+    cudaStream_t s[3];
+    if (check(swiglu_gateup_fwd_bwd_host_staging_size(chunk, n, dtype, depth, &staging_bytes),
+              "swiglu_gateup_fwd_bwd_host_staging_size") ||
+        check_cuda(cudaMalloc(&staging, staging_bytes), "cudaMalloc staging") ||
+        check_cuda(cudaMallocHost(&hx, bx), "cudaMallocHost") ||
+        check_cuda(cudaMallocHost(&hdy, by), "cudaMallocHost") ||
+        check_cuda(cudaMallocHost(&hy, by), "cudaMallocHost") ||
+        check_cuda(cudaMallocHost(&hdx, bx), "cudaMallocHost"))
+        return 1;
+    for (int i = 0; i < 3; ++i)
+        if (check_cuda(cudaStreamCreate(&s[i]), "cudaStreamCreate")) return 1;
+    memcpy(hx, host, bx);
+    memcpy(hdy, host + bx, by);
+    if (check(swiglu_gateup_fwd_bwd_host(hx, hdy, hy, hdx, rows, n, dtype, staging, staging_bytes,
+                                         chunk, depth, s[0], s[1], s[2]),
+              "swiglu_gateup_fwd_bwd_host"))
+        return 1;
     f = fopen(argv[5], "wb");
-    if (!f || fwrite(out, 1, by + 2 * bx, f) != by + 2 * bx) {
+    if (!f || fwrite(out, 1, by + 2 * bx, f) != by + 2 * bx || fwrite(hy, 1, by, f) != by ||
+        fwrite(hdx, 1, bx, f) != bx) {
         fprintf(stderr, "cannot write %s\n", argv[5]);
         return 2;
     }
     fclose(f);
+    for (int i = 0; i < 3; ++i) cudaStreamDestroy(s[i]);
+    cudaFreeHost(hx);
+    cudaFreeHost(hdy);
+    cudaFreeHost(hy);
+    cudaFreeHost(hdx);
+    cudaFree(staging);
     cudaFree(x);
     cudaFree(dy);
     cudaFree(y);

@@ -37,7 +37,8 @@ def test_header_declares_expected_calls():
          "swiglu_gateup_bias_bwd_workspace_size", "swiglu_gateup_bias_bwd",
          "swiglu_gateup_weighted_bias_fwd", "swiglu_gateup_weighted_bias_bwd_workspace_size",
          "swiglu_gateup_weighted_bias_bwd", "swiglu_gateup_bias_bwd_noalloc", "swiglu_fc1_fwd",
-         "swiglu_fc1_timeout_flag", "swiglu_status_string", "swiglu_last_cuda_error",
+         "swiglu_fc1_timeout_flag", "swiglu_gateup_fwd_bwd_host_staging_size",
+         "swiglu_gateup_fwd_bwd_host", "swiglu_status_string", "swiglu_last_cuda_error",
          "swiglu_abi_version"])
 
 
@@ -58,7 +59,7 @@ def test_status_strings(sw):
         s = sw.status_string(code)
         assert s and s != "unknown status"
     assert sw.status_string(-99) == "unknown status"
-    assert sw.lib.swiglu_abi_version() == 4
+    assert sw.lib.swiglu_abi_version() == 5
     assert sw.lib.swiglu_last_cuda_error() == 0
 
 
@@ -255,6 +256,44 @@ def test_fc1_rejections(sw):
     assert f(xo=Y + 64) == -5      # x_out over y
     assert f(xo=X) == -5
     assert sw.lib.swiglu_fc1_timeout_flag(None) == -1
+
+
+def test_host_pipeline_rejections(sw):
+    """swiglu_gateup_fwd_bwd_host checks everything before its first CUDA call
+    (the host addresses below are never touched)."""
+    import ctypes
+
+    HX, HDY, HY, HDX, ST = 0x1000_0000, 0x2000_0000, 0x3000_0000, 0x4000_0000, 0x50_0000_0000
+    size = ctypes.c_size_t(0)
+    assert sw.lib.swiglu_gateup_fwd_bwd_host_staging_size(16, 8, BF16, 3, ctypes.byref(size)) == 0
+    # three slots of x [16, 16], dy [16, 8], y [16, 8] bf16, each region 256-byte rounded
+    assert size.value == 3 * (512 + 256 + 256)
+    assert sw.lib.swiglu_gateup_fwd_bwd_host_staging_size(0, 8, BF16, 3, ctypes.byref(size)) == -3
+    assert sw.lib.swiglu_gateup_fwd_bwd_host_staging_size(16, 8, BF16, 9, ctypes.byref(size)) == -3
+    assert sw.lib.swiglu_gateup_fwd_bwd_host_staging_size(16, 8, 4, 3, ctypes.byref(size)) == -2
+    assert sw.lib.swiglu_gateup_fwd_bwd_host_staging_size(16, 8, BF16, 3, None) == -1
+    need = 3 * (512 + 256 + 256)
+
+    def h(**k):
+        return sw.lib.swiglu_gateup_fwd_bwd_host(
+            k.get("x", HX), k.get("dy", HDY), k.get("y", HY), k.get("dx", HDX), k.get("rows", 40),
+            k.get("n", 8), k.get("dt", BF16), k.get("st", ST), k.get("bytes", need),
+            k.get("chunk", 16), k.get("depth", 3), None, None, None)
+
+    assert h(rows=0, x=None, st=None) == 0
+    assert h(dt=9) == -2
+    assert h(n=-1) == -3
+    assert h(x=None) == -1
+    assert h(dx=None) == -1
+    assert h(st=None) == -1
+    assert h(chunk=0) == -3
+    assert h(depth=0) == -3
+    assert h(depth=9) == -3
+    assert h(bytes=need - 1) == -7          # staging too small
+    assert h(st=ST + 16) == -7              # staging not 256-byte aligned
+    assert h(y=HX + 64) == -5               # y inside x
+    assert h(dx=HDY) == -5                  # dx over dy
+    assert h(dx=HY + 32) == -5              # outputs overlap each other
 
 
 def test_import_fails_loudly_without_the_library(tmp_path):

@@ -1,7 +1,9 @@
 """The C ABI from a plain C99 program (tests/c_caller/main.c): the header
 compiles as C, and on a GPU the program -- linking libswiglu.so and the CUDA
 runtime, with device memory it allocates itself -- produces the oracle's
-results for the forward, the backward and the in-place backward."""
+results for the forward, the backward and the in-place backward, and the same
+bits again end to end from page-locked host buffers through
+swiglu_gateup_fwd_bwd_host."""
 import os
 import shutil
 import subprocess
@@ -67,7 +69,11 @@ def test_c_program_matches_oracle(tmp_path, name, rows):
     ny, nx = nrows * n, nrows * 2 * n
     y = vals[:ny].view(nrows, n)
     dx = vals[ny:ny + nx].view(nrows, 2 * n)
-    dx_in_place = vals[ny + nx:].view(nrows, 2 * n)
+    dx_in_place = vals[ny + nx:ny + 2 * nx].view(nrows, 2 * n)
+    y_host = vals[ny + 2 * nx:2 * ny + 2 * nx].view(nrows, n)
+    dx_host = vals[2 * ny + 2 * nx:].view(nrows, 2 * n)
     assert_parity(y, oracle.fwd(x), f"{name} C caller fwd")
     assert_parity(dx, oracle.bwd(dy, x), f"{name} C caller bwd")
     assert_bitwise(dx_in_place, dx, f"{name} C caller in place")
+    assert_bitwise(y_host, y, f"{name} C caller host pipeline y")
+    assert_bitwise(dx_host, dx, f"{name} C caller host pipeline dx")
