@@ -1,7 +1,7 @@
 """Bench of the fused gate-up SwiGLU on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline] [--no-extras]
     python bench.py --record-traffic NCU_CSV    # store an ncu DRAM capture
 
 One step = one forward plus one out-of-place backward (the "fwd+bwd" of the
@@ -314,10 +314,11 @@ def l2_bytes() -> int:
     return GB300_L2_BYTES
 
 
-def bench_config(w: W.Workload, world: int) -> dict:
+def bench_config(w: W.Workload, world: int, form: str = "plain") -> dict:
     """The workload description both arms print (identical dicts)."""
+    step = "fwd + out-of-place bwd" + ("" if form == "plain" else f" ({form} form)")
     return {"workload": w.name, "shape": list(w.shape), "ffn_local": w.n,
-            "storage_dtype": w.dtype, "step": "fwd + out-of-place bwd",
+            "storage_dtype": w.dtype, "step": step,
             "parallelism": f"independent replicas x{world}" if world > 1 else "one replica",
             "l2": l2_note(w)}
 
@@ -394,14 +395,45 @@ def ours_arm(args, w):
     dt_code = sw.SWIGLU_BF16 if w.dtype == W.BF16 else sw.SWIGLU_F32
     rows, n = w.rows, w.n
 
+    form = args.form
+    if form != "plain":
+        # the bias ([2n], storage dtype) and per-token weight (fp32) forms of
+        # the step, with their reduction workspace allocated once
+        gen = torch.Generator().manual_seed(11)
+        wts = torch.rand(rows, generator=gen).to(dev)
+        bias = (torch.randn(2 * n, generator=gen) * 0.5).to(x.dtype).to(dev)
+        dbias = torch.empty_like(bias)
+        dwv = torch.empty_like(wts)
+        size = (sw.bias_bwd_workspace_bytes if form == "bias"
+                else sw.weighted_bias_bwd_workspace_bytes)(rows, n)
+        wsp = torch.empty(max(16, size), dtype=torch.uint8, device=dev)
+
     def fwd():
-        st = lib.swiglu_gateup_fwd(x.data_ptr(), y.data_ptr(), rows, n, 2 * n, n, dt_code, sh)
+        if form == "plain":
+            st = lib.swiglu_gateup_fwd(x.data_ptr(), y.data_ptr(), rows, n, 2 * n, n, dt_code, sh)
+        elif form == "bias":
+            st = lib.swiglu_gateup_bias_fwd(x.data_ptr(), bias.data_ptr(), y.data_ptr(), rows, n,
+                                            2 * n, n, dt_code, sh)
+        else:
+            st = lib.swiglu_gateup_weighted_bias_fwd(x.data_ptr(), bias.data_ptr(), wts.data_ptr(),
+                                                     y.data_ptr(), rows, n, 2 * n, n, dt_code, sh)
         if st:
             raise sw.SwigluError(st, "fwd")
 
     def bwd(out, in_place):
-        st = lib.swiglu_gateup_bwd(dy.data_ptr(), x.data_ptr(), out.data_ptr(), rows, n, n, 2 * n,
-                                   2 * n, dt_code, 1 if in_place else 0, sh)
+        ip = 1 if in_place else 0
+        if form == "plain":
+            st = lib.swiglu_gateup_bwd(dy.data_ptr(), x.data_ptr(), out.data_ptr(), rows, n, n,
+                                       2 * n, 2 * n, dt_code, ip, sh)
+        elif form == "bias":
+            st = lib.swiglu_gateup_bias_bwd(dy.data_ptr(), x.data_ptr(), bias.data_ptr(),
+                                            out.data_ptr(), dbias.data_ptr(), wsp.data_ptr(),
+                                            wsp.numel(), rows, n, n, 2 * n, 2 * n, dt_code, ip, sh)
+        else:
+            st = lib.swiglu_gateup_weighted_bias_bwd(
+                dy.data_ptr(), x.data_ptr(), bias.data_ptr(), wts.data_ptr(), out.data_ptr(),
+                dbias.data_ptr(), dwv.data_ptr(), wsp.data_ptr(), wsp.numel(), rows, n, n, 2 * n,
+                2 * n, dt_code, ip, sh)
         if st:
             raise sw.SwigluError(st, "bwd")
 
@@ -464,11 +496,15 @@ def ours_arm(args, w):
     del x_saved
     ip_avg = max_over_ranks(statistics.mean(ip_ms))
 
-    extras = measure_extras(sw, w, x, dy, dev, stream, reps=min(K, 100))
-
+    # the end-to-end step runs before the extras: its page-locked host buffers
+    # are then allocated early, as a training process holds them for its whole
+    # life (allocated after the extras' compilation and GEMM runs they copied
+    # about 7 % slower on the same box)
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(sw, w, x, dy, dev, K=min(K, 20), barrier=barrier, reduce=max_over_ranks)
+
+    extras = None if args.no_extras else measure_extras(sw, w, x, dy, dev, stream, reps=min(K, 100))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -485,13 +521,14 @@ def ours_arm(args, w):
     fb, bb = w.fwd_bytes(), w.bwd_bytes()
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     bwd_gbs = gbs(bb, bwd_avg)
-    traffic = stored_traffic("bwd", w.name)
+    # stored counters describe the plain form's kernels only
+    traffic = stored_traffic("bwd", w.name) if args.form == "plain" else None
     line = {
         "metric": METRIC, "value": round(ms_step, 4), "unit": "ms", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": bench_config(w, ws),
+        "config": bench_config(w, ws, args.form),
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
         "bwd_in_place_ms": round(ip_avg, 4),
         "fwd_gbs": round(gbs(fb, fwd_avg), 1), "bwd_gbs": round(bwd_gbs, 1),
@@ -502,8 +539,10 @@ def ours_arm(args, w):
                                  "peak_gbs": peak, "peak_source": peak_src},
         "frac_of_8000_gbs": {"fwd": round(gbs(fb, fwd_avg) / 8000, 4),
                              "fwdbwd": round(gbs(fb + bb, fwd_avg + bwd_avg) / 8000, 4)},
-        "ncu_frac_of_8000_gbs": ncu_fractions(w),
-        "roofline": {"bound": "hbm", "kernel": "swiglu_bwd_kernel (out of place)",
+        "ncu_frac_of_8000_gbs": ncu_fractions(w) if args.form == "plain" else None,
+        "roofline": {"bound": "hbm",
+                     "kernel": "swiglu_bwd_kernel (out of place)" if args.form == "plain"
+                     else f"{args.form} backward (tile kernel + reductions)",
                      "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(bwd_gbs / peak, 4), "peak_source": peak_src,
                      "traffic": traffic, "algorithmic_bytes": bb},
@@ -517,12 +556,23 @@ def ours_arm(args, w):
     ranks.close()
 
 
+MIN_TIMED_MS = 5.0  # shortest span of back-to-back launches one figure is averaged over
+
+
 def _event_ms(fn, stream, reps):
-    """Mean CUDA-event time of fn() on `stream` over `reps` launches (after 3
-    warm-up calls)."""
+    """Mean CUDA-event time of fn() on `stream` over at least `reps` launches
+    and at least MIN_TIMED_MS of them (after 3 warm-up calls): short kernels
+    get enough launches for a stable mean."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(3):
         fn()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(3):
+        fn()
+    b.record(stream)
+    b.synchronize()
+    est = max(a.elapsed_time(b) / 3, 1e-3)
+    reps = int(min(5000, max(reps, -(-MIN_TIMED_MS // est))))
     a.record(stream)
     for _ in range(reps):
         fn()
@@ -645,6 +695,8 @@ def measure_extras(sw, w, x, dy, dev, stream, reps):
     fc1 = measure_fc1(sw, dev, stream, reps=max(5, min(reps, 20)))
 
     return {
+        "timing": f"CUDA events over back-to-back launches of one kind: each figure is the mean "
+                  f"over at least its 'reps' launches and at least {MIN_TIMED_MS:g} ms of them",
         "unfused_torch_eager": {
             "what": "eager PyTorch ops on the same buffers: fwd chunk + silu * up, bwd chunk + "
                     "the two formulas + cat (intermediates rounded to the storage dtype)",
@@ -860,6 +912,11 @@ def main():
     ap.add_argument("--workload", default=W.HEADLINE, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the step alone (the command the kernel profiles are taken on)")
+    ap.add_argument("--form", choices=["plain", "bias", "weighted_bias"], default="plain",
+                    help="the entry points of the timed step: plain (the headline), or the bias / "
+                         "per-token weights + bias forms")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.json from an ncu CSV log of this bench and exit")
@@ -870,6 +927,8 @@ def main():
         print(json.dumps({k: v["bytes_per_launch"] for k, v in out.items() if k != "_note"}))
         return
     if args.impl == "reference":
+        if args.form != "plain":
+            raise SystemExit("--impl reference times the plain form only")
         reference_arm(args, w)
     else:
         ours_arm(args, w)

@@ -105,12 +105,24 @@ constexpr Policy kFwdModePolicy = {32, 4, 4, 8};  // bias and / or row weights
 // one-pass 32-byte grid; the Llama-like (235 MB) and large-FFN shapes are
 // faster on the one-pass grid.
 constexpr int64_t kFwdSmallBytes = (int64_t)128 << 20;
-constexpr Policy kBwdPolicy = {16, 0, 0, 6};
+// Backward, plain form: 32-byte packs, one per thread, on a one-pass grid of
+// 128-thread CTAs (16-byte packs: two per thread): Megatron shape 51.1 us
+// against 53.0 us with two 16-byte packs per thread on 256-thread CTAs,
+// Llama-like 165.3 against 168.0, large FFN 373 against 378 (256-thread CTAs
+// with one 32-byte pack: 54.3 / 176.2 / 394.8).  The bias and per-token-weight
+// forms stay at 16-byte packs (their tile and row kernels are built on them).
+constexpr Policy kBwdPolicy = {32, 0, 0, 6};
+constexpr int kBwdModeMaxPack = 16;
 // The per-token-weighted backward is one CTA per row, persistent over rows.
 constexpr Policy kRowPolicy = {16, 3, 3, 6};
-// The bias tile kernel is launched as one wave of this many CTAs per SM (its
-// __launch_bounds__ minimum); the workspace size follows from it.
-constexpr int kBiasCtasPerSm = 3;
+// The bias tile kernel is launched as one wave of this many CTAs per SM; the
+// workspace size follows from it.  Swept with the cp.async ring
+// (BiasStages) over 1.5 - 6 CTAs per SM on the large-FFN and Llama-like
+// shapes: the bias form did best at 2 (407.6 / 189.0 us against 424.7 /
+// 196.7 us for the ring-less kernel at 3), the weights + bias form at 3
+// (429.0 / 202.7 us against 475.2 / 221.1; 466 / 215 at 2).
+constexpr int kBiasCtasPerSm = 2;
+constexpr int kWeightedBiasCtasPerSm = 3;
 
 // Resident CTAs per SM to launch with, 0 for a one-pass grid.
 constexpr int ctas_cap(const Policy &p, int pack_bytes) {
@@ -218,17 +230,18 @@ struct BwdArgs {
 };
 
 // Row groups of the bias backward: enough (column tile, row group) CTAs to
-// fill every SM with kBiasCtasPerSm of them (the tile kernel's launch bound),
-// once.
+// fill every SM with kBiasCtasPerSm (with weights: kWeightedBiasCtasPerSm) of
+// them, once.
 struct BiasPlan {
     int64_t tiles, groups, rows_per_group;
     size_t workspace_bytes;
 };
 
-BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {  // rows, n >= 1
+BiasPlan bias_plan(int64_t rows, int64_t n, int sms, bool weighted) {  // rows, n >= 1
     BiasPlan b;
     b.tiles = (n + swiglu::kBiasTileCols - 1) / swiglu::kBiasTileCols;
-    int64_t groups = ((int64_t)sms * kBiasCtasPerSm) / b.tiles;
+    const int per_sm = weighted ? kWeightedBiasCtasPerSm : kBiasCtasPerSm;
+    int64_t groups = ((int64_t)sms * per_sm) / b.tiles;
     if (groups < 1) groups = 1;
     if (groups > rows) groups = rows;
     b.rows_per_group = (rows + groups - 1) / groups;
@@ -241,7 +254,7 @@ BiasPlan bias_plan(int64_t rows, int64_t n, int sms) {  // rows, n >= 1
 // boundary), one fp32 dw partial per (row, column tile).  False when the size
 // does not fit size_t.
 bool weighted_bias_workspace(int64_t rows, int64_t n, int sms, size_t &dw_offset, size_t &bytes) {
-    const BiasPlan b = bias_plan(rows, n, sms);
+    const BiasPlan b = bias_plan(rows, n, sms, true);
     dw_offset = (b.workspace_bytes + 15) / 16 * 16;
     size_t cells, dw_bytes;
     if (__builtin_mul_overflow((size_t)rows, (size_t)b.tiles, &cells)) return false;
@@ -384,26 +397,28 @@ swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
 template <typename E, int VEC, bool IN_PLACE>
 swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
+    constexpr int cap = ctas_cap(kBwdPolicy, E::kBytes * VEC);
+    // one-pass grids run 128-thread CTAs, persistent ones kThreads
+    constexpr int T = cap == 0 ? 128 : swiglu::kThreads;
     static std::atomic<int> occ[kMaxDevices];
     auto kernel = swiglu::swiglu_bwd_kernel<E, VEC, U, IN_PLACE,
-                                            IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore>;
+                                            IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore, T>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
     int per_sm = 0;
-    constexpr int cap = ctas_cap(kBwdPolicy, E::kBytes * VEC);
     if (cap > 0) {
-        e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, per_sm);
+        e = ctas_per_sm(kernel, T, d, occ, per_sm);
         if (e != cudaSuccess) return cuda_fail(e);
         if (per_sm > cap) per_sm = cap;
     }
     const int64_t nvec = a.n / VEC;
-    const int64_t grid = grid_for<U>(a.rows * nvec, d, per_sm);
-    const int64_t step = grid * U * swiglu::kThreads;
+    const int64_t grid = grid_for<U, T>(a.rows * nvec, d, per_sm);
+    const int64_t step = grid * U * T;
     swiglu::BwdParams p = bwd_params(a, VEC);
     p.step_q = step / nvec;
     p.step_r = (int32_t)(step % nvec);
-    kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(p);
+    kernel<<<(unsigned)grid, T, 0, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
@@ -430,16 +445,39 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
+// Rows in flight through the bias tile kernel's cp.async ring (0: plain
+// register loads), for 16-byte packs; see swiglu_bwd_bias_kernel.
+template <typename E, bool WEIGHTED>
+struct BiasStages {
+    static constexpr int value = 2;
+};
+// Rows of dw partial sums the weights + bias tile kernel batches per barrier
+// (16 leaves room for the ring at 3 CTAs per SM; same speed as 32).
+constexpr int kDwBatch = 16;
+
 template <typename E, int VEC, bool IN_PLACE, bool WEIGHTED>
 swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
+    constexpr int STAGES = E::kBytes * VEC == 16 ? BiasStages<E, WEIGHTED>::value : 0;
+    constexpr int ring = swiglu::swiglu_bias_ring_bytes<VEC, E::kBytes, STAGES>();
     auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
                                                  IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore,
-                                                 WEIGHTED>;
+                                                 WEIGHTED, STAGES, kDwBatch>;
+    static std::atomic<int> opted_in[kMaxDevices];
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    const BiasPlan b = bias_plan(a.rows, a.n, d.sms);
-    kernel<<<(unsigned)(b.tiles * b.groups), swiglu::kThreads, 0, stream>>>(
+    if (ring > 0) {
+        // dynamic shared memory beyond 48 KiB (with the static batch buffer)
+        // needs the kernel's opt-in, once per device
+        const bool cacheable = d.id >= 0 && d.id < kMaxDevices;
+        if (!cacheable || opted_in[d.id].load(std::memory_order_relaxed) == 0) {
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (cacheable) opted_in[d.id].store(1, std::memory_order_relaxed);
+        }
+    }
+    const BiasPlan b = bias_plan(a.rows, a.n, d.sms, WEIGHTED);
+    kernel<<<(unsigned)(b.tiles * b.groups), swiglu::kThreads, ring, stream>>>(
         bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
@@ -459,9 +497,12 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
 
 template <typename E, int VEC, bool IN_PLACE>
 swiglu_status_t launch_bwd(const BwdArgs &a, cudaStream_t stream) {
-    if (a.mode == swiglu::kWeight) return launch_bwd_weighted<E, VEC, IN_PLACE>(a, stream);
-    if (a.mode == swiglu::kBias) return launch_bwd_bias<E, VEC, IN_PLACE, false>(a, stream);
-    if (a.mode == swiglu::kBiasWeight) return launch_bwd_bias<E, VEC, IN_PLACE, true>(a, stream);
+    // packs wider than kBwdModeMaxPack only ever reach here for the plain form
+    if constexpr (E::kBytes * VEC <= kBwdModeMaxPack) {
+        if (a.mode == swiglu::kWeight) return launch_bwd_weighted<E, VEC, IN_PLACE>(a, stream);
+        if (a.mode == swiglu::kBias) return launch_bwd_bias<E, VEC, IN_PLACE, false>(a, stream);
+        if (a.mode == swiglu::kBiasWeight) return launch_bwd_bias<E, VEC, IN_PLACE, true>(a, stream);
+    }
     return launch_bwd_plain<E, VEC, IN_PLACE>(a, stream);
 }
 
@@ -503,7 +544,8 @@ swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     const int64_t strides[5] = {a.dy.stride, a.g.stride, a.u.stride, a.dg.stride, a.du.stride};
     const void *ptrs[7] = {a.dy.p, a.g.p, a.u.p, a.dg.p, a.du.p, a.bias_g, a.bias_u};
     const int np = (a.mode & swiglu::kBias) ? 7 : 5;
-    const int vec = pick_vec(E::kBytes, kBwdPolicy.max_pack_bytes, a.n, strides, 5, ptrs, np);
+    const int max_pack = a.mode == swiglu::kPlain ? kBwdPolicy.max_pack_bytes : kBwdModeMaxPack;
+    const int vec = pick_vec(E::kBytes, max_pack, a.n, strides, 5, ptrs, np);
     if (a.mode == swiglu::kPlain && vec * E::kBytes <= kSegMaxPackBytes) {
         const Operand in[3] = {a.dy, a.g, a.u};
         const Operand out[2] = {a.dg, a.du};
@@ -635,7 +677,7 @@ swiglu_status_t bias_bwd_impl(const void *dy, const void *x, const void *bias, c
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    size_t need = bias_plan(rows, n, d.sms).workspace_bytes, dw_offset = 0;
+    size_t need = bias_plan(rows, n, d.sms, weighted).workspace_bytes, dw_offset = 0;
     if (weighted && !weighted_bias_workspace(rows, n, d.sms, dw_offset, need))
         return SWIGLU_ERR_SHAPE;
     if (workspace_bytes < need) return SWIGLU_ERR_WORKSPACE;
@@ -773,7 +815,7 @@ swiglu_status_t swiglu_gateup_bias_bwd_workspace_size(int64_t rows, int64_t n, s
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    *bytes = bias_plan(rows, n, d.sms).workspace_bytes;
+    *bytes = bias_plan(rows, n, d.sms, false).workspace_bytes;
     return SWIGLU_OK;
 }
 
@@ -1005,7 +1047,7 @@ extern "C" swiglu_status_t swiglu_gateup_bias_bwd_noalloc(
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (bias_plan(rows, n, d.sms).workspace_bytes > SWIGLU_NOALLOC_SCRATCH_BYTES)
+    if (bias_plan(rows, n, d.sms, false).workspace_bytes > SWIGLU_NOALLOC_SCRATCH_BYTES)
         return SWIGLU_ERR_WORKSPACE;
     void *scratch = nullptr;
     e = noalloc_scratch(d.id, &scratch);

@@ -141,6 +141,19 @@ SWIGLU_DEFINE_ST(kStNoAlloc, "st.global.L1::no_allocate")
 SWIGLU_DEFINE_ST(kStPlain, "st.global")
 #undef SWIGLU_DEFINE_ST
 
+// Asynchronous 16-byte copies from global into shared memory (cached in L2
+// only), grouped by commit_group and awaited by wait_group: the issuing
+// thread may read its own copies once the wait returns.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------ data types ---
 // Element i of a pack <-> fp32.  Storage rounding is round-to-nearest-even.
 struct F32 {
@@ -253,8 +266,29 @@ __device__ __forceinline__ float two_sum(float a, float b, float &e) {
 // enough to need it.
 // kMayDeep = false: the caller knows g >= -64 (or NaN), so the deep-tail
 // scaling is left out (scale is exactly 1; same bits as the general form).
+//
+// Storage types with the hardware exponential (bf16), g >= -64 or NaN: with
+// t = e^-g <= e^64 nothing overflows, so
+//   s = 1 / (1 + t),  1 - s = 1 - s (rounded),  silu' = s (1 + g (1 - s))
+// without |g|, a sign test or selects.  Error, relative to one bf16 step
+// (2^-8): t carries the rounding of its exponent argument (at most 2^-18 ln 2
+// relative, at |g| = 64) and ex2.approx / rcp.approx their ~2^-22, so s is
+// within ~3e-6 relative; 1 - s adds an absolute 2^-24, which only matters
+// where 1 + g (1 - s) is small: at the bf16 gates nearest silu's root
+// (|1 + g (1 - s)| >= 0.0028) it stays below 1e-4 relative, and for large
+// positive g the term g (1 - s) is below 1e-6 against 1.  So every result is
+// within a small fraction of a bf16 step of the exact value before its single
+// rounding.  g < -64 takes the scaled form below.
 template <typename E, bool kGrad, bool kMayDeep = true>
 __device__ __forceinline__ Act activation(float g, float g_lo = 0.0f) {
+    if (E::kFastExp && !(E::kDeepScale && kMayDeep && g < -64.0f)) {
+        const float s = rcp_approx(__fadd_rn(1.0f, ex2_approx(__fmul_rn(g, -kLog2e))));
+        Act o;
+        o.silu = __fmul_rn(g, s);
+        o.scale = 1.0f;
+        o.dsilu = kGrad ? __fmul_rn(s, __fmaf_rn(g, __fsub_rn(1.0f, s), 1.0f)) : 0.0f;
+        return o;
+    }
     const float a = fabsf(g);
     const bool pos = g >= 0.0f;
     // deep: for g < -64, t * 2^64 < 2^-24, so 1 + t rounds to 1 with or
@@ -475,13 +509,10 @@ __global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_ker
             if (r[k] < p.rows) {
                 uint32_t o[NW] = {};
                 float yv[VEC];
-                // the pack-level split paid for the plain and the weights +
-                // bias forms and cost 5-6 % for bias or weights alone (same
-                // bits either way)
-                constexpr bool kSplit = MODE == kPlain || MODE == kBiasWeight;
-                const bool deep = !kSplit ? true
-                                  : (MODE & kBias) ? pack_has_deep_biased<E, VEC>(g[k], bg[k])
-                                                   : pack_has_deep<E, VEC>(g[k]);
+                // packs with no gate below -64 (all but the deep tail) take
+                // the activation without the deep-tail test (same bits)
+                const bool deep = (MODE & kBias) ? pack_has_deep_biased<E, VEC>(g[k], bg[k])
+                                                 : pack_has_deep<E, VEC>(g[k]);
                 if (deep)
                     fwd_pack<E, VEC, MODE, true>(g[k], u[k], bg[k], bu[k], wr[k], yv);
                 else
@@ -574,9 +605,10 @@ __global__ void __launch_bounds__(T) swiglu_bwd_kernel(const BwdParams p) {
 // forms its operand pointers once per segment and reaches its K columns
 // (t, t + T, ..., so a warp touches consecutive elements) through constant
 // offsets, loading all of them before computing any.  The arithmetic is
-// fwd_pack / bwd_pack on one-element packs, so the bits equal those of every
-// other kernel; each column is read and written by one thread, so the
-// in-place backward is the same kernel with coherent loads.
+// fwd_pack / bwd_pack on one-element packs, split on the deep tail like the
+// pack kernels, so the bits equal those of every other kernel; each column is
+// read and written by one thread, so the in-place backward is the same kernel
+// with coherent loads.
 enum : int { kSegFwd = 0, kSegBwd = 1 };
 
 struct SegParams {
@@ -620,13 +652,19 @@ __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
             if (i < live) {
                 if (MODE == kSegFwd) {
                     float yv[1];
-                    fwd_pack<E, 1, kPlain, true>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
+                    if (pack_has_deep<E, 1>(&w[0][i]))
+                        fwd_pack<E, 1, kPlain, true>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
+                    else
+                        fwd_pack<E, 1, kPlain, false>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
                     uint32_t o[1] = {0u};
                     store_pack<E, 1>(o, yv);
                     St<EB, kStStream>::run(op[0] + i * T * EB, o);
                 } else {
                     float gv[1], uv[1];
-                    bwd_pack<E, 1, true>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
+                    if (pack_has_deep<E, 1>(&w[1][i]))
+                        bwd_pack<E, 1, true>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
+                    else
+                        bwd_pack<E, 1, false>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
                     uint32_t og[1] = {0u}, ou[1] = {0u};
                     store_pack<E, 1>(og, gv);
                     store_pack<E, 1>(ou, uv);
@@ -785,20 +823,39 @@ __device__ __forceinline__ void bias_pack(const uint32_t *d, const uint32_t *g, 
 // one barrier, each warp finishes rows of the batch: a lane adds the sums of
 // threads lane, lane + 32, ... in order, then a shuffle tree adds the lanes.
 // The row loop itself carries no cross-thread step.
-template <typename E, int VEC, bool IN_PLACE, int LD, int ST, bool WEIGHTED = false>
+//
+// STAGES > 0 (16-byte packs only): instead of loading each row's packs into
+// registers and waiting for them, every thread copies its own packs of the
+// next STAGES - 1 rows into a private slice of a shared-memory ring with
+// cp.async and reads each row back from there when it computes it.  Loads in
+// flight then hold no registers, so more rows are in flight at the occupancy
+// the registers allow; no barrier is needed, since a thread only ever reads
+// the ring slots it filled itself (cp.async.wait_group orders them).  Ring:
+// STAGES x 3 operands x PPT packs x kThreads threads x 16 bytes of dynamic
+// shared memory (swiglu_bias_ring_bytes).
+template <int VEC, int E_BYTES, int STAGES>
+constexpr int swiglu_bias_ring_bytes() {
+    return STAGES * 3 * (kBiasTileCols / (kThreads * VEC)) * kThreads * E_BYTES * VEC;
+}
+
+template <typename E, int VEC, bool IN_PLACE, int LD, int ST, bool WEIGHTED = false, int STAGES = 0,
+          int DW_BATCH = 32>
 __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
                                                                       int64_t rows_per_group) {
     constexpr int MODE = WEIGHTED ? kBiasWeight : kBias;
-    constexpr int kDwBatch = 32;
+    constexpr int kDwBatch = DW_BATCH;
     __shared__ float wpart[WEIGHTED ? kDwBatch : 1][WEIGHTED ? kThreads : 1];
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     constexpr int PPT = kBiasTileCols / (kThreads * VEC);  // packs per thread per row and half
     static_assert(PPT >= 1 && PPT * kThreads * VEC == kBiasTileCols, "tile / pack mismatch");
+    static_assert(STAGES == 0 || (B == 16 && STAGES >= 2), "the cp.async ring moves 16-byte packs");
     // rows whose loads are issued together: keeps about as many bytes in flight
-    // per thread as the streaming backward
-    constexpr int RU = PPT >= 2 ? 1 : 2;
+    // per thread as the streaming backward (the ring keeps STAGES - 1 rows in
+    // flight instead)
+    constexpr int RU = STAGES > 0 ? 1 : (PPT >= 2 ? 1 : 2);
+    extern __shared__ __align__(16) unsigned char bias_ring[];
     using L = Ld<B, LD>;
     using S = St<B, ST>;
     const int32_t tile = blockIdx.x % tiles;
@@ -822,18 +879,66 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
         for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
     }
+    // ring slot of (stage, operand, pack) for this thread
+    auto ring_at = [&](int st, int x, int k) -> unsigned char * {
+        return bias_ring + ((size_t)((st * 3 + x) * PPT + k) * kThreads + threadIdx.x) * 16;
+    };
+    // start the copies of row r's packs into ring stage st
+    auto ring_fill = [&](int64_t r, int st) {
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            if (c[k] < p.nvec) {
+                cp_async16(ring_at(st, 0, k), static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B);
+                cp_async16(ring_at(st, 1, k), static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B);
+                cp_async16(ring_at(st, 2, k), static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B);
+            }
+        }
+    };
+    int stage = 0;  // ring stage of the current row
+    if (STAGES > 0) {
+#pragma unroll
+        for (int st = 0; st < (STAGES > 0 ? STAGES - 1 : 0); ++st) {
+            if (r0 + st < r1) ring_fill(r0 + st, st);
+            cp_async_commit();
+        }
+    }
     int slot = 0;  // rows of the current dw batch held in wpart
     for (int64_t rb = r0; rb < r1; rb += RU) {
         uint32_t d[RU][PPT][NW], g[RU][PPT][NW], u[RU][PPT][NW];
-#pragma unroll
-        for (int q = 0; q < RU; ++q) {
-            const int64_t r = rb + q;
+        if (STAGES > 0) {
+            // refill the stage the previous row used, then wait for this row
+            const int64_t ahead = rb + (STAGES > 0 ? STAGES - 1 : 0);
+            if (ahead < r1) ring_fill(ahead, stage == 0 ? STAGES - 1 : stage - 1);
+            cp_async_commit();
+            cp_async_wait<(STAGES > 0 ? STAGES - 1 : 0)>();
 #pragma unroll
             for (int k = 0; k < PPT; ++k) {
-                if (r < r1 && c[k] < p.nvec) {
-                    L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[q][k]);
-                    L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[q][k]);
-                    L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[q][k]);
+                if (c[k] < p.nvec) {
+                    const uint4 qd = *reinterpret_cast<const uint4 *>(ring_at(stage, 0, k));
+                    const uint4 qg = *reinterpret_cast<const uint4 *>(ring_at(stage, 1, k));
+                    const uint4 qu = *reinterpret_cast<const uint4 *>(ring_at(stage, 2, k));
+                    const uint32_t wd[4] = {qd.x, qd.y, qd.z, qd.w}, wg[4] = {qg.x, qg.y, qg.z, qg.w},
+                                   wu[4] = {qu.x, qu.y, qu.z, qu.w};
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) {
+                        d[0][k][i] = wd[i];
+                        g[0][k][i] = wg[i];
+                        u[0][k][i] = wu[i];
+                    }
+                }
+            }
+            stage = stage + 1 == STAGES ? 0 : stage + 1;
+        } else {
+#pragma unroll
+            for (int q = 0; q < RU; ++q) {
+                const int64_t r = rb + q;
+#pragma unroll
+                for (int k = 0; k < PPT; ++k) {
+                    if (r < r1 && c[k] < p.nvec) {
+                        L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[q][k]);
+                        L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[q][k]);
+                        L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[q][k]);
+                    }
                 }
             }
         }
@@ -880,6 +985,7 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
             }
         }
     }
+    if (STAGES > 0) cp_async_wait<0>();
     const int64_t n = (int64_t)p.nvec * VEC;
     float *part = p.partial + group * 2 * n;
 #pragma unroll

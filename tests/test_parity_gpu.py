@@ -354,7 +354,8 @@ def test_more_than_2_32_elements(sw):
     xsub, dysub = _cols(x, J, n).cpu(), dy[:, J].cpu()
     bsub = torch.cat([bias[J], bias[n + J]]).cpu()
     dx64, db64, _ = oracle.weighted_bias_bwd(dysub.double(), xsub.double(), bsub.double(), wts.cpu())
-    assert_reduction(torch.cat([db[J], db[n + J]]), db64, dx64.abs().sum(0), _bias_depth(rows, n),
+    assert_reduction(torch.cat([db[J], db[n + J]]), db64, dx64.abs().sum(0),
+                     _bias_depth(rows, n, weighted=True),
                      "2^32 dbias columns")
     del x, dy, dx
     torch.cuda.empty_cache()

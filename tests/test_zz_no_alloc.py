@@ -5,9 +5,11 @@ device memory (engines that plan all memory ahead and forbid allocation
 mid-step, plugin hosts that own the allocator, latency-bound paths that cannot
 take cudaMalloc's synchronisation): its scratch is a fixed array inside the
 library.  Its results must match the workspace entry point's, within the
-tolerances the other tests use, on two calls in a row (the second call must not
-see anything the first left in the shared array), and a problem too large for
-the fixed array must be refused without touching the outputs.
+tolerances the other tests use, and the oracle's (dx element by element, dbias
+within the summation bound of the other bias tests), on two calls in a row
+(the second call must not see anything the first left in the shared array),
+and a problem too large for the fixed array must be refused without touching
+the outputs.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes on its own.
@@ -16,6 +18,7 @@ failure has already run every other test; it also passes on its own.
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from helpers import assert_parity
 
@@ -66,6 +69,7 @@ def test_noalloc_matches_workspace_entry_point_twice(sw, name, rows):
         torch.cuda.synchronize()
         assert_parity(dx, ref_dx.cpu(), f"{name} no-alloc dx")
         assert_parity(db, ref_db.cpu(), f"{name} no-alloc dbias")
+        _against_oracle(dy, x, bias, dx, db, f"{name} no-alloc")
     # the in-place form through the same entry point
     x, dy, bias = first
     ref_dx, ref_db = sw.swiglu_gateup_bias_bwd(dy, x, bias)
@@ -75,6 +79,19 @@ def test_noalloc_matches_workspace_entry_point_twice(sw, name, rows):
     torch.cuda.synchronize()
     assert_parity(xi, ref_dx.cpu(), f"{name} no-alloc in-place dx")
     assert_parity(db, ref_db.cpu(), f"{name} no-alloc in-place dbias")
+
+
+def _against_oracle(dy, x, bias, dx, db, what):
+    """dx element by element against the oracle's once-rounded value, dbias
+    against the exact column sums within the fixed-order fp32 summation bound
+    the other bias tests use."""
+    from test_bias_weighted_gpu import _bias_depth, assert_reduction
+
+    dy_c, x_c, b_c = dy.cpu(), x.cpu(), bias.cpu()
+    rows, n = dy_c.shape
+    assert_parity(dx, oracle.bias_bwd(dy_c, x_c, b_c)[0], f"{what} dx vs oracle")
+    dx64, db64 = oracle.bias_bwd(dy_c.double(), x_c.double(), b_c.double())
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), f"{what} dbias vs oracle")
 
 
 def test_noalloc_refuses_what_does_not_fit(sw):
