@@ -82,16 +82,13 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 // 105.5, Megatron shape 31.9 against 34.0: CTAs that start in address order
 // keep the DRAM access window compact, where persistent CTAs drift apart.
 // With 16-byte packs (two in flight) 6 CTAs per SM did best.  The forward
-// variants with a bias or row weights keep persistent grids of 4 CTAs per SM:
-// on the one-pass grid they ran 3-11 % slower.  Backward (both forms), two
-// 16-byte packs in flight: once the pack-level deep-tail test took ~5
-// instructions per element out of the common path, the one-pass grid won as
-// well -- large FFN 386.0 us against 399-418 us at 3 CTAs per SM, Llama-like
-// 172.2 against 177.6, in place 389.2 against 403.5.  Narrow packs (4 bytes
-// or less: odd n, misaligned rows) of the plain and two-tensor forms go to the
-// row-segment kernels (SegShape below); for the bias and per-token-weight
-// forms they want persistent CTAs with more threads: four packs in flight and
-// 8 (forward) / 6 (backward) CTAs per SM.
+// variants with a bias or row weights: see kFwdModePolicy.  Backward, plain
+// form: one-pass as well (see kBwdPolicy; at 3 CTAs per SM the large FFN ran
+// 399-418 us against 386 on one pass, before the 32-byte packs).  Narrow
+// packs (4 bytes or less: odd n, misaligned rows) of the plain and two-tensor
+// forms go to the row-segment kernels (SegShape below); for the bias and
+// per-token-weight forms they want persistent CTAs with more threads: four
+// packs in flight and 8 (forward) / 6 (backward) CTAs per SM.
 struct Policy {
     int max_pack_bytes;
     int ctas_wide;    // 32-byte packs; 0 = a one-pass grid
@@ -99,7 +96,12 @@ struct Policy {
     int ctas_narrow;  // packs of 4 bytes or less
 };
 constexpr Policy kFwdPolicy = {32, 0, 6, 8};
-constexpr Policy kFwdModePolicy = {32, 4, 4, 8};  // bias and / or row weights
+// Bias or row weights alone: one pass as well (large FFN 225.4 / 223.3 us
+// against 258.0 / 254.3 us at 4 CTAs per SM; Llama-like 101.4 / 100.2 against
+// 109.5 / 108.9).  Both together: persistent at 4 CTAs per SM (234.8 us
+// against 249.9 on one pass of 256-thread CTAs and 325.8 of 128-thread ones).
+constexpr Policy kFwdModePolicy = {32, 0, 4, 8};
+constexpr Policy kFwdBiasWeightPolicy = {32, 4, 4, 8};
 // Forward outputs below this size (the Megatron ffn-4096 shape's 67 MB among
 // them) use 16-byte packs at 6 CTAs per SM: 29.4 us against 33.1 us on the
 // one-pass 32-byte grid; the Llama-like (235 MB) and large-FFN shapes are
@@ -265,7 +267,10 @@ bool weighted_bias_workspace(int64_t rows, int64_t n, int sms, size_t &dw_offset
 template <typename E, int VEC, int MODE>
 swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
-    constexpr int cap = ctas_cap(MODE == swiglu::kPlain ? kFwdPolicy : kFwdModePolicy, E::kBytes * VEC);
+    constexpr int cap = ctas_cap(MODE == swiglu::kPlain        ? kFwdPolicy
+                                 : MODE == swiglu::kBiasWeight ? kFwdBiasWeightPolicy
+                                                               : kFwdModePolicy,
+                                 E::kBytes * VEC);
     // the one-pass grid runs 128-thread CTAs: 0.5-1.7 % faster than 256 on the
     // large-FFN and Llama-like shapes
     constexpr int T = cap == 0 ? 128 : swiglu::kThreads;

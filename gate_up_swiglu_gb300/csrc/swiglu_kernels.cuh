@@ -474,7 +474,10 @@ __device__ __forceinline__ void fwd_pack(const uint32_t *g, const uint32_t *u, c
 }
 
 // T: threads per CTA (kThreads unless the launch policy picks another).
-template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain, int T = kThreads>
+// SPLIT: test each pack for the deep tail and run the common case without
+// the per-element test (same bits either way).
+template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain, int T = kThreads,
+          bool SPLIT = true>
 __global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
@@ -511,8 +514,9 @@ __global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_ker
                 float yv[VEC];
                 // packs with no gate below -64 (all but the deep tail) take
                 // the activation without the deep-tail test (same bits)
-                const bool deep = (MODE & kBias) ? pack_has_deep_biased<E, VEC>(g[k], bg[k])
-                                                 : pack_has_deep<E, VEC>(g[k]);
+                const bool deep = !SPLIT ? true
+                                  : (MODE & kBias) ? pack_has_deep_biased<E, VEC>(g[k], bg[k])
+                                                   : pack_has_deep<E, VEC>(g[k]);
                 if (deep)
                     fwd_pack<E, VEC, MODE, true>(g[k], u[k], bg[k], bu[k], wr[k], yv);
                 else

@@ -9,7 +9,9 @@ The tolerance follows through y = silu(g) * u (|silu'| <= 1.1):
     |y - y_exact| <= one bf16 step at |y_exact| + 1.1 gamma A_g |u| + |silu(g)| gamma A_u
                      + (gamma A_g)(gamma A_u)
 and for the stored fc1: one bf16 step + gamma A.  Most elements must also
-land within one bf16 step of the exact value (a sharper check than the bound).
+land within one bf16 step of the exact value (a sharper check than the bound);
+each test prints the measured share and records it as the junit property
+within_one_bf16_step.
 """
 import pytest
 import torch
@@ -62,6 +64,9 @@ def _check(y_gpu, fc1_gpu, X, Wt, rows, what):
         tol_f = _step(ref.abs()) + gam * A
         badf = (f - ref).abs() > tol_f
         assert int(badf.sum()) == 0, f"{what}: {int(badf.sum())} fc1 values out of bound"
+    print(f"{what}: {frac:.5f} of {d.numel()} y values within one bf16 step of the oracle, "
+          f"largest distance {int(d.max())} steps")
+    return frac
 
 
 def _inputs(M, n, K, seed):
@@ -75,14 +80,14 @@ def _inputs(M, n, K, seed):
 @pytest.mark.parametrize("M,n,K", [(128, 128, 64), (256, 256, 512), (200, 384, 72),
                                    (1, 128, 8), (333, 128, 1000), (260, 200, 96), (64, 8, 64),
                                    (130, 136, 128)])
-def test_fc1_small_against_oracle(sw, M, n, K):
+def test_fc1_small_against_oracle(sw, M, n, K, record_property):
     X, Wt = _inputs(M, n, K, seed=M + n + K)
     y, fc1 = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda(), return_fc1=True)
     y_only = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda())
     torch.cuda.synchronize()
     assert sw.fc1_timeout_flag() == 0
     rows = torch.arange(M)
-    _check(y, fc1, X, Wt, rows, f"fc1 M{M} n{n} K{K}")
+    record_property("within_one_bf16_step", _check(y, fc1, X, Wt, rows, f"fc1 M{M} n{n} K{K}"))
     assert torch.equal(y_only, y), "y must not depend on whether fc1 is stored"
     # the stored fc1 feeds the separate activation kernel to the same y bits
     # up to the bf16 rounding of fc1 (a different, coarser computation): check
@@ -91,7 +96,7 @@ def test_fc1_small_against_oracle(sw, M, n, K):
     assert int((bf16_ordered(y2.cpu()) - bf16_ordered(y.cpu())).abs().max()) <= 64
 
 
-def test_fc1_llama_shape_sampled(sw):
+def test_fc1_llama_shape_sampled(sw, record_property):
     """Llama-3-8B MLP fc1: X [8192, 4096] x W [28672, 4096] -> y [8192, 14336];
     sampled rows against the exact values."""
     M, K, n = 8192, 4096, 14336
@@ -102,7 +107,7 @@ def test_fc1_llama_shape_sampled(sw):
     torch.cuda.synchronize()
     assert sw.fc1_timeout_flag() == 0
     rows = torch.tensor([0, 1, 127, 128, 4095, 8190, 8191])
-    _check(y, fc1, X.cpu(), Wt.cpu(), rows, "fc1 llama")
+    record_property("within_one_bf16_step", _check(y, fc1, X.cpu(), Wt.cpu(), rows, "fc1 llama"))
 
 
 @pytest.mark.parametrize("in_place", [False, True])
