@@ -823,11 +823,16 @@ def l2_note(w: W.Workload) -> str:
     return f"inputs {inputs / 2**20:.0f} MiB fit in L2 {l2 / 2**20:.0f} MiB: L2-resident timing"
 
 
-def link_rates(dev, nbytes: int = 1 << 30) -> dict:
-    """Host link rates from pinned memory, same run: one nbytes copy each way
-    alone, then both directions at once on two streams (GB/s, best of 3)."""
-    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+def link_rates(dev, h_in: torch.Tensor, h_out: torch.Tensor) -> dict:
+    """Host link rates of the given page-locked buffers, same run: h_in copied
+    to the device alone, the device copied into h_out alone, then both at once
+    on two streams (GB/s each way, best of 3).  The duplex rate depends on
+    where the buffers land in host memory (149-170 GB/s on one box across
+    buffer sets), so it is measured on the very buffers the end-to-end step
+    uses."""
+    nbytes = min(h_in.numel() * h_in.element_size(), h_out.numel() * h_out.element_size())
+    src = h_in.view(-1).view(torch.uint8)[:nbytes]
+    dst = h_out.view(-1).view(torch.uint8)[:nbytes]
     d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -844,16 +849,17 @@ def link_rates(dev, nbytes: int = 1 << 30) -> dict:
 
     def both():
         with torch.cuda.stream(s1):
-            d_in.copy_(h_in, non_blocking=True)
+            d_in.copy_(src, non_blocking=True)
         with torch.cuda.stream(s2):
-            h_out.copy_(d_out, non_blocking=True)
+            dst.copy_(d_out, non_blocking=True)
 
-    t_in = best(lambda: d_in.copy_(h_in, non_blocking=True))
-    t_out = best(lambda: h_out.copy_(d_out, non_blocking=True))
+    t_in = best(lambda: d_in.copy_(src, non_blocking=True))
+    t_out = best(lambda: dst.copy_(d_out, non_blocking=True))
     t_both = best(both)
     return {"h2d_gbs": round(nbytes / t_in / 1e9, 1), "d2h_gbs": round(nbytes / t_out / 1e9, 1),
             "duplex_each_way_gbs": round(nbytes / t_both / 1e9, 1),
-            "copy_bytes": nbytes, "how": "pinned host memory, host clock, best of 3"}
+            "copy_bytes": nbytes,
+            "how": "the step's own pinned x (in) and dx (out) buffers, host clock, best of 3"}
 
 
 def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
@@ -891,8 +897,9 @@ def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
     ms = reduce((time.perf_counter() - t0) * 1e3 / K)
     h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
     d2h = yh.numel() * yh.element_size() + dxh.numel() * dxh.element_size()
-    del xh, dyh, yh, dxh, staging
-    link = link_rates(dev)
+    del staging
+    link = link_rates(dev, xh, dxh)
+    del xh, dyh, yh, dxh
     # the floor set by the link: the larger direction at the measured duplex rate
     floor_ms = max(h2d, d2h) / (link["duplex_each_way_gbs"] * 1e9) * 1e3
     return {"value": round(ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,

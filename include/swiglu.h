@@ -235,10 +235,10 @@ swiglu_status_t swiglu_gateup_weighted_bias_bwd(
  *   - A problem whose scratch need (swiglu_gateup_bias_bwd_workspace_size)
  *     exceeds SWIGLU_NOALLOC_SCRATCH_BYTES is rejected with
  *     SWIGLU_ERR_WORKSPACE before anything is launched.  For any rows and n
- *     the need is at most max(3 * SMs * 2048 * 8, 8 n) bytes, SMs being the
- *     device's multiprocessor count (7.1 MiB on a 152-SM GB300, so every
+ *     the need is at most max(2 * SMs * 2048 * 8, 8 n) bytes, SMs being the
+ *     device's multiprocessor count (4.75 MiB on a 152-SM GB300, so every
  *     n <= 2^21 fits); it reaches 8 n only when one row group spans the
- *     whole matrix (n above 3 * SMs * 2048).
+ *     whole matrix (n above 2 * SMs * 2048).
  *   - The first call in a CUDA context (per device, and again after a
  *     cudaDeviceReset) looks up the array's device address with that device
  *     current (cudaGetSymbolAddress); make that first call before any stream
