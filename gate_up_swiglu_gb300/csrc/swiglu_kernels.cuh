@@ -210,13 +210,15 @@ struct BF16 {
 };
 
 // ------------------------------------------------------------------ math ---
-// sigmoid(g) and 1 - sigmoid(g) come from t = exp(-|g|) in (0, 1]:
+// fp32 (and the deep bf16 tail): sigmoid(g) and 1 - sigmoid(g) come from
+// t = exp(-|g|) in (0, 1]:
 //   g >= 0:  s = 1 / (1 + t),  1 - s = t / (1 + t)
 //   g <  0:  s = t / (1 + t),  1 - s = 1 / (1 + t)
 // so neither the exponential overflows nor 1 - s cancels, for any finite g.
-// Explicit _rn operations fix the rounding of every step (no contraction), so
-// all instantiations -- in particular the in-place and out-of-place backward
-// -- produce the same bits.
+// bf16 with g >= -64 takes a shorter form that one bf16 step tolerates (see
+// activation below).  Explicit _rn operations fix the rounding of every step
+// (no contraction), so all instantiations -- in particular the in-place and
+// out-of-place backward -- produce the same bits.
 
 constexpr float kLn2x64 = 44.3614195558365f;  // 64 ln 2
 constexpr float kTwoPowMinus64 = 5.421010862427522e-20f;  // 2^-64, exact
