@@ -317,24 +317,32 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
 // backward 53.3 us (K = 8; 55.3 at T = 256), bf16 forward 135.2 us at K = 16
 // (141.4 at K = 8), backward 219.6 us at K = 8.  The per-element walk these
 // kernels replace took 44.5 / 62.4 us on the fp32 workload.
-template <typename E, int MODE>
+// The forward of the bias forms keeps K = 8 for bf16 too (the bias values of
+// 16 columns took the kernel to 101 registers and half the speed).
+template <typename E, int MODE, int FMODE = swiglu::kPlain>
 struct SegShape {
     static constexpr int K = 8, T = 128, per_sm = 0;
 };
 template <>
-struct SegShape<swiglu::BF16, swiglu::kSegFwd> {
+struct SegShape<swiglu::BF16, swiglu::kSegFwd, swiglu::kPlain> {
+    static constexpr int K = 16, T = 128, per_sm = 0;
+};
+template <>
+struct SegShape<swiglu::BF16, swiglu::kSegFwd, swiglu::kWeight> {
     static constexpr int K = 16, T = 128, per_sm = 0;
 };
 
 // Operands: fwd in = {g, u}, out = {y}; bwd in = {dy, g, u}, out = {dg, du}.
-template <typename E, int MODE, bool IN_PLACE>
+// FMODE: the forward's variant; bias_g / bias_u / w as in FwdArgs.
+template <typename E, int MODE, bool IN_PLACE, int FMODE = swiglu::kPlain>
 swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t rows, int64_t n,
-                              cudaStream_t stream) {
-    using Sh = SegShape<E, MODE>;
+                              cudaStream_t stream, const void *bias_g = nullptr,
+                              const void *bias_u = nullptr, const float *w = nullptr) {
+    using Sh = SegShape<E, MODE, FMODE>;
     constexpr int NIN = MODE == swiglu::kSegFwd ? 2 : 3;
     constexpr int NOUT = MODE == swiglu::kSegFwd ? 1 : 2;
     auto kernel = swiglu::swiglu_rowseg_kernel<E, MODE, Sh::K, Sh::T,
-                                               IN_PLACE ? kLoadInPlace : kLoadOutOfPlace>;
+                                               IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, FMODE>;
     static std::atomic<int> occ[kMaxDevices];
     Device d;
     cudaError_t e = current_device(d);
@@ -359,6 +367,9 @@ swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t row
         p.out[x] = x < NOUT ? static_cast<char *>(const_cast<void *>(out[x].p)) : nullptr;
         p.out_stride[x] = x < NOUT ? out[x].stride * E::kBytes : 0;
     }
+    p.bias_g = static_cast<const char *>(bias_g);
+    p.bias_u = static_cast<const char *>(bias_u);
+    p.w = w;
     p.n = n;
     p.segments = segments;
     p.div_chunks = make_fast_div((uint64_t)chunks);
@@ -369,8 +380,9 @@ swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t row
 }
 
 // Calls whose operands share no pack wider than this many bytes take the
-// row-segment kernels (plain and two-tensor forms; the bias and
-// per-token-weight forms keep the streaming kernels).
+// row-segment kernels (the forward of every form, the plain and two-tensor
+// backward; the bias and per-token-weight backward keep their tile and row
+// kernels).
 constexpr int kSegMaxPackBytes = 4;
 
 swiglu::BwdParams bwd_params(const BwdArgs &a, int vec) {
@@ -451,7 +463,9 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
 }
 
 // Rows in flight through the bias tile kernel's cp.async ring (0: plain
-// register loads), for 16-byte packs; see swiglu_bwd_bias_kernel.
+// register loads), for 16-byte packs; see swiglu_bwd_bias_kernel.  (With
+// 4-byte packs -- fp32, odd n -- a 2-row ring ran 139 us against 97 us
+// without on the odd-width workload's bias backward.)
 template <typename E, bool WEIGHTED>
 struct BiasStages {
     static constexpr int value = 2;
@@ -532,9 +546,21 @@ swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const bool small = a.mode == swiglu::kPlain && a.rows * a.n * E::kBytes < kFwdSmallBytes;
     const int vec = pick_vec(E::kBytes, small ? 16 : kFwdPolicy.max_pack_bytes, a.n, strides, 3,
                              ptrs, np);
-    if (a.mode == swiglu::kPlain && vec * E::kBytes <= kSegMaxPackBytes) {
+    if (vec * E::kBytes <= kSegMaxPackBytes) {
         const Operand in[2] = {a.g, a.u};
-        return launch_rowseg<E, swiglu::kSegFwd, false>(in, &a.y, a.rows, a.n, st);
+        switch (a.mode) {
+            case swiglu::kBias:
+                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBias>(in, &a.y, a.rows, a.n, st,
+                                                                               a.bias_g, a.bias_u);
+            case swiglu::kWeight:
+                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kWeight>(
+                    in, &a.y, a.rows, a.n, st, nullptr, nullptr, a.w);
+            case swiglu::kBiasWeight:
+                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBiasWeight>(
+                    in, &a.y, a.rows, a.n, st, a.bias_g, a.bias_u, a.w);
+            default:
+                return launch_rowseg<E, swiglu::kSegFwd, false>(in, &a.y, a.rows, a.n, st);
+        }
     }
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);

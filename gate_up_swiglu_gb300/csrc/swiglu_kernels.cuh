@@ -16,7 +16,8 @@
 // CTA per U * T packs, T threads per CTA) or as a persistent grid of a few
 // resident CTAs per SM, as the host's launch policy decides.  Shapes whose
 // operands share no pack wider than 4 bytes (odd n, misaligned rows) go to
-// the row-segment kernels further down.
+// the row-segment kernels further down (the forward of every form and the
+// plain backward).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -147,6 +148,20 @@ SWIGLU_DEFINE_ST(kStPlain, "st.global")
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+// 4- and 8-byte copies (cached in L1 as well: the L2-only form takes 16 bytes)
+template <int B>
+__device__ __forceinline__ void cp_async_small(void *smem_dst, const void *gsrc) {
+    static_assert(B == 4 || B == 8, "cp.async copies 4, 8 or 16 bytes");
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(gsrc), "n"(B) : "memory");
+}
+template <int B>
+__device__ __forceinline__ void cp_async_pack(void *smem_dst, const void *gsrc) {
+    if constexpr (B == 16)
+        cp_async16(smem_dst, gsrc);
+    else
+        cp_async_small<B>(smem_dst, gsrc);
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -622,17 +637,23 @@ struct SegParams {
     int64_t in_stride[3];   // row strides in bytes
     char *out[2];           // fwd: y; bwd: dg, du
     int64_t out_stride[2];
+    const char *bias_g;     // forward with kBias: [n] bias of each half (column 0)
+    const char *bias_u;
+    const float *w;         // forward with kWeight: [rows]
     int64_t n;
     int64_t segments;       // rows * chunks
     FastDiv div_chunks;     // division by chunks
     int32_t chunks;         // segments per row: ceil(n / (K * T))
 };
 
-template <typename E, int MODE, int K, int T, int LD>
+// FMODE: the forward's variant (kPlain, kBias, kWeight, kBiasWeight); the
+// backward is the plain form only.
+template <typename E, int MODE, int K, int T, int LD, int FMODE = kPlain>
 __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
     constexpr int EB = E::kBytes;
     constexpr int NIN = MODE == kSegFwd ? 2 : 3;
     constexpr int NOUT = MODE == kSegFwd ? 1 : 2;
+    static_assert(MODE == kSegFwd || FMODE == kPlain, "the backward row segments are the plain form");
     for (int64_t seg = blockIdx.x; seg < p.segments; seg += gridDim.x) {
         const int64_t r = fast_div(seg, p.div_chunks);
         const int64_t c = (seg - r * p.chunks) * (int64_t)(K * T) + threadIdx.x;
@@ -643,13 +664,19 @@ __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
 #pragma unroll
         for (int x = 0; x < NIN; ++x) ip[x] = p.in[x] + r * p.in_stride[x] + c * EB;
         uint32_t w[NIN][K];
+        uint32_t bgw[K], buw[K];  // kBias: the bias of each column (reread by every row: L1)
 #pragma unroll
         for (int i = 0; i < K; ++i) {
             if (i < live) {
 #pragma unroll
                 for (int x = 0; x < NIN; ++x) Ld<EB, LD>::run(ip[x] + i * T * EB, &w[x][i]);
+                if (FMODE & kBias) {
+                    Ld<EB, kLdCached>::run(p.bias_g + (c + i * T) * EB, &bgw[i]);
+                    Ld<EB, kLdCached>::run(p.bias_u + (c + i * T) * EB, &buw[i]);
+                }
             }
         }
+        const float wr = (FMODE & kWeight) ? __ldg(p.w + r) : 1.0f;
         char *op[NOUT];
 #pragma unroll
         for (int x = 0; x < NOUT; ++x) op[x] = p.out[x] + r * p.out_stride[x] + c * EB;
@@ -658,10 +685,12 @@ __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
             if (i < live) {
                 if (MODE == kSegFwd) {
                     float yv[1];
-                    if (pack_has_deep<E, 1>(&w[0][i]))
-                        fwd_pack<E, 1, kPlain, true>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
+                    const bool deep = (FMODE & kBias) ? pack_has_deep_biased<E, 1>(&w[0][i], &bgw[i])
+                                                      : pack_has_deep<E, 1>(&w[0][i]);
+                    if (deep)
+                        fwd_pack<E, 1, FMODE, true>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
                     else
-                        fwd_pack<E, 1, kPlain, false>(&w[0][i], &w[1][i], nullptr, nullptr, 1.0f, yv);
+                        fwd_pack<E, 1, FMODE, false>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
                     uint32_t o[1] = {0u};
                     store_pack<E, 1>(o, yv);
                     St<EB, kStStream>::run(op[0] + i * T * EB, o);
@@ -830,15 +859,16 @@ __device__ __forceinline__ void bias_pack(const uint32_t *d, const uint32_t *g, 
 // threads lane, lane + 32, ... in order, then a shuffle tree adds the lanes.
 // The row loop itself carries no cross-thread step.
 //
-// STAGES > 0 (16-byte packs only): instead of loading each row's packs into
+// STAGES > 0 (16-byte packs; the ring also works with 4 and 8): instead of loading each row's packs into
 // registers and waiting for them, every thread copies its own packs of the
 // next STAGES - 1 rows into a private slice of a shared-memory ring with
 // cp.async and reads each row back from there when it computes it.  Loads in
 // flight then hold no registers, so more rows are in flight at the occupancy
 // the registers allow; no barrier is needed, since a thread only ever reads
 // the ring slots it filled itself (cp.async.wait_group orders them).  Ring:
-// STAGES x 3 operands x PPT packs x kThreads threads x 16 bytes of dynamic
-// shared memory (swiglu_bias_ring_bytes).
+// STAGES x 3 operands x PPT packs x kThreads threads x one pack of dynamic
+// shared memory (swiglu_bias_ring_bytes); consecutive threads own consecutive
+// slots, so the reads back are free of bank conflicts.
 template <int VEC, int E_BYTES, int STAGES>
 constexpr int swiglu_bias_ring_bytes() {
     return STAGES * 3 * (kBiasTileCols / (kThreads * VEC)) * kThreads * E_BYTES * VEC;
@@ -856,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     constexpr int NW = (B + 3) / 4;
     constexpr int PPT = kBiasTileCols / (kThreads * VEC);  // packs per thread per row and half
     static_assert(PPT >= 1 && PPT * kThreads * VEC == kBiasTileCols, "tile / pack mismatch");
-    static_assert(STAGES == 0 || (B == 16 && STAGES >= 2), "the cp.async ring moves 16-byte packs");
+    static_assert(STAGES == 0 || ((B == 4 || B == 8 || B == 16) && STAGES >= 2),
+                  "the cp.async ring moves 4-, 8- or 16-byte packs");
     // rows whose loads are issued together: keeps about as many bytes in flight
     // per thread as the streaming backward (the ring keeps STAGES - 1 rows in
     // flight instead)
@@ -887,17 +918,35 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     }
     // ring slot of (stage, operand, pack) for this thread
     auto ring_at = [&](int st, int x, int k) -> unsigned char * {
-        return bias_ring + ((size_t)((st * 3 + x) * PPT + k) * kThreads + threadIdx.x) * 16;
+        return bias_ring + ((size_t)((st * 3 + x) * PPT + k) * kThreads + threadIdx.x) * B;
     };
     // start the copies of row r's packs into ring stage st
     auto ring_fill = [&](int64_t r, int st) {
+        if constexpr (STAGES > 0) {
 #pragma unroll
-        for (int k = 0; k < PPT; ++k) {
-            if (c[k] < p.nvec) {
-                cp_async16(ring_at(st, 0, k), static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B);
-                cp_async16(ring_at(st, 1, k), static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B);
-                cp_async16(ring_at(st, 2, k), static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B);
+            for (int k = 0; k < PPT; ++k) {
+                if (c[k] < p.nvec) {
+                    cp_async_pack<B>(ring_at(st, 0, k), static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B);
+                    cp_async_pack<B>(ring_at(st, 1, k), static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B);
+                    cp_async_pack<B>(ring_at(st, 2, k), static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B);
+                }
             }
+        }
+    };
+    // the NW words of a ring slot
+    auto ring_read = [&](const unsigned char *slot, uint32_t *w) {
+        if constexpr (B == 16) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(slot);
+            w[0] = q.x;
+            w[1] = q.y;
+            w[2] = q.z;
+            w[3] = q.w;
+        } else if constexpr (B == 8) {
+            const uint2 q = *reinterpret_cast<const uint2 *>(slot);
+            w[0] = q.x;
+            w[1] = q.y;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t *>(slot);
         }
     };
     int stage = 0;  // ring stage of the current row
@@ -920,17 +969,9 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
             for (int k = 0; k < PPT; ++k) {
                 if (c[k] < p.nvec) {
-                    const uint4 qd = *reinterpret_cast<const uint4 *>(ring_at(stage, 0, k));
-                    const uint4 qg = *reinterpret_cast<const uint4 *>(ring_at(stage, 1, k));
-                    const uint4 qu = *reinterpret_cast<const uint4 *>(ring_at(stage, 2, k));
-                    const uint32_t wd[4] = {qd.x, qd.y, qd.z, qd.w}, wg[4] = {qg.x, qg.y, qg.z, qg.w},
-                                   wu[4] = {qu.x, qu.y, qu.z, qu.w};
-#pragma unroll
-                    for (int i = 0; i < NW; ++i) {
-                        d[0][k][i] = wd[i];
-                        g[0][k][i] = wg[i];
-                        u[0][k][i] = wu[i];
-                    }
+                    ring_read(ring_at(stage, 0, k), d[0][k]);
+                    ring_read(ring_at(stage, 1, k), g[0][k]);
+                    ring_read(ring_at(stage, 2, k), u[0][k]);
                 }
             }
             stage = stage + 1 == STAGES ? 0 : stage + 1;
