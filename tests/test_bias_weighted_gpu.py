@@ -359,3 +359,19 @@ def test_bias_and_weighted_layouts(sw, case):
     dx.fill_(-7.0)
     assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
                        dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"
+    # the three forward forms into a guarded y with the same padding and
+    # misalignment (narrow packs take the row-segment kernel)
+    yb, yg = _guard(rows, n, dyp, mis, dt, -7.0)
+    yb0 = yb.clone()
+    for what, run, ref in (
+            ("bias", lambda: sw.swiglu_gateup_bias_fwd(x, bias, yg), oracle.bias_fwd(x_c, bias_c)),
+            ("weighted", lambda: sw.swiglu_gateup_weighted_fwd(x, wts, yg), oracle.weighted_fwd(x_c, w_c)),
+            ("weighted bias", lambda: sw.swiglu_gateup_weighted_bias_fwd(x, bias, wts, yg),
+             oracle.weighted_bias_fwd(x_c, bias_c, w_c))):
+        run()
+        torch.cuda.synchronize()
+        assert_parity(yg, ref, f"{what} fwd into a guarded y")
+        yg.fill_(-7.0)
+        assert torch.equal(yb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                           yb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), \
+            f"{what} fwd guard bands"
