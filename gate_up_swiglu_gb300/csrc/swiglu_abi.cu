@@ -500,16 +500,17 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
         bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    int64_t rgrid = (2 * a.n + swiglu::kThreads - 1) / swiglu::kThreads;
-    if (rgrid > (int64_t)d.sms * 8) rgrid = (int64_t)d.sms * 8;
-    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)rgrid, swiglu::kThreads, 0, stream>>>(
-        a.partial, b.groups, 2 * a.n, a.dbias);
+    constexpr int RT = swiglu::kReduceThreads;
+    int64_t rgrid = (2 * a.n + RT - 1) / RT;
+    if (rgrid > (int64_t)d.sms * 16) rgrid = (int64_t)d.sms * 16;
+    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)rgrid, RT, 0, stream>>>(a.partial, b.groups,
+                                                                              2 * a.n, a.dbias);
     e = cudaGetLastError();
     if (e != cudaSuccess || !WEIGHTED) return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
-    int64_t wgrid = (a.rows + swiglu::kThreads - 1) / swiglu::kThreads;
-    if (wgrid > (int64_t)d.sms * 8) wgrid = (int64_t)d.sms * 8;
-    swiglu::swiglu_dw_reduce_kernel<<<(unsigned)wgrid, swiglu::kThreads, 0, stream>>>(
-        a.partial_dw, a.rows, (int32_t)b.tiles, a.dw);
+    int64_t wgrid = (a.rows + RT - 1) / RT;
+    if (wgrid > (int64_t)d.sms * 16) wgrid = (int64_t)d.sms * 16;
+    swiglu::swiglu_dw_reduce_kernel<<<(unsigned)wgrid, RT, 0, stream>>>(a.partial_dw, a.rows,
+                                                                        (int32_t)b.tiles, a.dw);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }

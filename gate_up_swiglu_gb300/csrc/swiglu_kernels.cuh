@@ -1047,16 +1047,37 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     }
 }
 
+// Threads per CTA of the two reduction passes below (small CTAs: the grids
+// have one thread per column or row, fewer than the SMs hold).
+constexpr int kReduceThreads = 128;
+
+// Sum of the `count` floats at p, p + stride, ..., added in that order; the
+// loads go out eight at a time so a long chain of groups does not wait on
+// one load latency per term.
+__device__ __forceinline__ float ordered_sum(const float *p, int64_t count, int64_t stride) {
+    float s = 0.0f;
+    int64_t q = 0;
+    for (; q + 8 <= count; q += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = p[(q + i) * stride];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = __fadd_rn(s, v[i]);
+    }
+    for (; q < count; ++q) s = __fadd_rn(s, p[q * stride]);
+    return s;
+}
+
 // Bias backward, second pass: dbias[k] = sum over groups of partial[group][k],
 // in group order, rounded once to the storage type.
 template <typename E>
-__global__ void __launch_bounds__(kThreads) swiglu_bias_reduce_kernel(const float *partial,
-                                                                      int64_t groups, int64_t two_n,
-                                                                      void *dbias) {
-    for (int64_t k = (int64_t)blockIdx.x * kThreads + threadIdx.x; k < two_n;
-         k += (int64_t)gridDim.x * kThreads) {
-        float s = 0.0f;
-        for (int64_t q = 0; q < groups; ++q) s = __fadd_rn(s, partial[q * two_n + k]);
+__global__ void __launch_bounds__(kReduceThreads) swiglu_bias_reduce_kernel(const float *partial,
+                                                                            int64_t groups,
+                                                                            int64_t two_n,
+                                                                            void *dbias) {
+    for (int64_t k = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; k < two_n;
+         k += (int64_t)gridDim.x * kReduceThreads) {
+        const float s = ordered_sum(partial + k, groups, two_n);
         uint32_t w[1] = {0};
         E::put(w, 0, s);
         if (E::kBytes == 4)
@@ -1067,14 +1088,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_bias_reduce_kernel(const floa
 }
 
 // dw[r] = sum over column tiles of partial_dw[r, tile], in tile order.
-static __global__ void __launch_bounds__(kThreads)
+static __global__ void __launch_bounds__(kReduceThreads)
     swiglu_dw_reduce_kernel(const float *partial_dw, int64_t rows, int32_t tiles, float *dw) {
-    for (int64_t r = (int64_t)blockIdx.x * kThreads + threadIdx.x; r < rows;
-         r += (int64_t)gridDim.x * kThreads) {
-        float s = 0.0f;
-        for (int32_t t = 0; t < tiles; ++t) s = __fadd_rn(s, partial_dw[r * tiles + t]);
-        dw[r] = s;
-    }
+    for (int64_t r = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; r < rows;
+         r += (int64_t)gridDim.x * kReduceThreads)
+        dw[r] = ordered_sum(partial_dw + r * tiles, tiles, 1);
 }
 
 }  // namespace swiglu
