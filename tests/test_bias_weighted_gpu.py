@@ -44,10 +44,29 @@ def _step(dtype, mag: torch.Tensor) -> torch.Tensor:
     return torch.clamp(mag, min=2.0 ** -126) * 2.0 ** -mant
 
 
-def assert_reduction(gpu, exact, abs_sum, depth, what):
+def _term_bound(elem, abs_sum, count):
+    """The error the summed terms may carry before the summation: each term is
+    one of the kernel's fp32 gradients (or dw terms), computed from inputs of
+    dtype `elem`.  fp32: each is held to max(2e-6 |t|, 1e-7) of the exact
+    value (the elementwise tolerance), so the terms together to at most
+    2e-6 sum|t| + 1e-7 count.  bf16: the hardware exponential and reciprocal
+    keep each within 2^-17 relative (the kernels' sigmoid error is below
+    3e-6 relative), so 2^-17 sum|t|."""
+    if elem == torch.float32:
+        return 2e-6 * abs_sum + 1e-7 * count
+    if elem == torch.bfloat16:
+        return 2.0 ** -17 * abs_sum
+    raise TypeError(elem)
+
+
+def assert_reduction(gpu, exact, abs_sum, depth, what, *, elem, count):
+    """A fixed-order fp32 sum of `count` kernel terms against the exact sum of
+    the exact terms: the terms' own error (_term_bound) plus the summation's,
+    (depth + 6) 2^-24 sum|t| for `depth` chained additions, plus one step of
+    the output type."""
     dtype = gpu.dtype
     gpu = gpu.cpu().double()
-    bound = (depth + 6) * U32 * abs_sum
+    bound = (depth + 6) * U32 * abs_sum + _term_bound(elem, abs_sum, count)
     tol = bound + _step(dtype, exact.abs() + bound)
     bad = (gpu - exact).abs() > tol
     nb = int(bad.sum())
@@ -97,7 +116,7 @@ def test_weighted_matches_oracle(sw, name, rows):
     terms = (dy64 * oracle.fwd(x64)).abs().sum(1)
     exact = (dy64 * oracle.fwd(x64)).sum(1)
     assert torch.allclose(dw64.double(), exact, rtol=1e-6, atol=1e-30)
-    assert_reduction(dw, exact, terms, w_.n / 256 + 13, f"{name} dw")
+    assert_reduction(dw, exact, terms, w_.n / 256 + 13, f"{name} dw", elem=x.dtype, count=w_.n)
 
 
 @pytest.mark.parametrize("name,rows", CASES)
@@ -119,7 +138,8 @@ def test_bias_matches_oracle(sw, name, rows):
     assert_bitwise(xi, dx, "bias in-place dx")
     assert_bitwise(dbi, db, "bias in-place dbias")
     dx64, db64 = oracle.bias_bwd(dy.double(), x.double(), bias.double())
-    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(r, n), f"{name} dbias")
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(r, n), f"{name} dbias",
+                     elem=x.dtype, count=r)
 
 
 def _wb_dw_depth(n):
@@ -135,9 +155,10 @@ def _check_weighted_bias(dy_c, x_c, bias_c, w_c, y, dx, db, dw, what):
     x64, dy64, b64 = x_c.double(), dy_c.double(), bias_c.double()
     dx64, db64, _ = oracle.weighted_bias_bwd(dy64, x64, b64, w_c)
     assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n, weighted=True),
-                     f"{what} dbias")
+                     f"{what} dbias", elem=x_c.dtype, count=rows)
     t = dy64 * oracle.bias_fwd(x64, b64)
-    assert_reduction(dw, t.sum(1), t.abs().sum(1), _wb_dw_depth(n), f"{what} dw")
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), _wb_dw_depth(n), f"{what} dw", elem=x_c.dtype,
+                     count=n)
 
 
 @pytest.mark.parametrize("name,rows", CASES)
@@ -176,8 +197,9 @@ def test_weighted_bias_matches_oracle(sw, name, rows):
     # summation bound of its own order around the exact sum
     dx64, db64 = oracle.bias_bwd(dy.double(), x.double(), bias.double())
     assert_reduction(db1, db64, dx64.abs().sum(0), _bias_depth(r, n, weighted=True),
-                     "unit weights dbias (weights + bias form)")
-    assert_reduction(dbb, db64, dx64.abs().sum(0), _bias_depth(r, n), "unit weights dbias (bias form)")
+                     "unit weights dbias (weights + bias form)", elem=x.dtype, count=r)
+    assert_reduction(dbb, db64, dx64.abs().sum(0), _bias_depth(r, n), "unit weights dbias (bias form)",
+                     elem=x.dtype, count=r)
 
 
 def test_weighted_bias_full_size(sw):
@@ -197,7 +219,8 @@ def test_weighted_bias_full_size(sw):
     assert_parity(y[idx], oracle.weighted_bias_fwd(xs, bc, ws), "full weighted bias fwd rows")
     assert_parity(dx[idx], oracle.weighted_bias_bwd(dys, xs, bc, ws)[0], "full weighted bias dx rows")
     t = dys.double() * oracle.bias_fwd(xs.double(), bc.double())
-    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "full dw rows")
+    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "full dw rows",
+                     elem=x.dtype, count=n)
     cols = torch.tensor(sorted(set([0, 1, 2047, 2048, n - 1] +
                                    torch.randperm(n, generator=g)[:59].tolist())))
     cc = cols.cuda()
@@ -207,7 +230,7 @@ def test_weighted_bias_full_size(sw):
     dx64, db64, _ = oracle.weighted_bias_bwd(dysub.double(), xsub.double(), bsub.double(), wts.cpu())
     got = torch.cat([db[cc], db[n + cc]])
     assert_reduction(got, db64, dx64.abs().sum(0), _bias_depth(w_.rows, n, weighted=True),
-                     "full dbias columns")
+                     "full dbias columns", elem=x.dtype, count=w_.rows)
 
 
 def test_bias_full_size_columns(sw):
@@ -234,7 +257,8 @@ def test_bias_full_size_columns(sw):
     bsub = torch.cat([bias[cc], bias[n + cc]]).cpu()
     dx64, db64 = oracle.bias_bwd(dysub.double(), xsub.double(), bsub.double())
     got = torch.cat([db[cc], db[n + cc]])
-    assert_reduction(got, db64, dx64.abs().sum(0), _bias_depth(w_.rows, n), "full dbias columns")
+    assert_reduction(got, db64, dx64.abs().sum(0), _bias_depth(w_.rows, n), "full dbias columns",
+                     elem=x.dtype, count=w_.rows)
 
 
 def test_weighted_full_size_rows(sw):
@@ -249,7 +273,8 @@ def test_weighted_full_size_rows(sw):
     assert_parity(y[idx], oracle.weighted_fwd(xs, ws), "full weighted fwd rows")
     assert_parity(dx[idx], oracle.weighted_bwd(dys, xs, ws)[0], "full weighted dx rows")
     t = dys.double() * oracle.fwd(xs.double())
-    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), w_.n / 256 + 13, "full dw rows")
+    assert_reduction(dw[idx], t.sum(1), t.abs().sum(1), w_.n / 256 + 13, "full dw rows",
+                     elem=x.dtype, count=w_.n)
 
 
 def test_empty_and_workspace_errors(sw):
@@ -335,7 +360,8 @@ def test_bias_and_weighted_layouts(sw, case):
     assert_parity(dx, rdx, "bias dx")
     assert_parity(y, oracle.bias_fwd(x_c, bias_c), "bias fwd")
     dx64, db64 = oracle.bias_bwd(dy_c.double(), x_c.double(), bias_c.double())
-    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), "bias dbias")
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), "bias dbias", elem=dt,
+                     count=rows)
     dx.fill_(-7.0)
     assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
                        dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"
@@ -347,7 +373,7 @@ def test_bias_and_weighted_layouts(sw, case):
     assert_parity(dx, rdx, "weighted dx")
     assert_parity(yw, oracle.weighted_fwd(x_c, w_c), "weighted fwd")
     t = dy_c.double() * oracle.fwd(x_c.double())
-    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, "weighted dw")
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, "weighted dw", elem=dt, count=n)
     dx.fill_(-7.0)
     assert torch.equal(dxb.view(torch.int16 if dt == torch.bfloat16 else torch.int32),
                        dxb0.view(torch.int16 if dt == torch.bfloat16 else torch.int32)), "guard bands"

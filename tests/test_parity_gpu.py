@@ -349,14 +349,15 @@ def test_more_than_2_32_elements(sw):
     torch.cuda.synchronize()
     assert_parity(dx[R], oracle.weighted_bias_bwd(dys, xs, bc, ws)[0], "2^32 weighted bias dx")
     t = dys.double() * oracle.bias_fwd(xs.double(), bc.double())
-    assert_reduction(dw[R], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "2^32 dw rows")
+    assert_reduction(dw[R], t.sum(1), t.abs().sum(1), _wb_dw_depth(n), "2^32 dw rows",
+                     elem=torch.bfloat16, count=n)
     J = torch.tensor([0, 1, 2047, 2048, 4095, 4096, n - 1], device="cuda")
     xsub, dysub = _cols(x, J, n).cpu(), dy[:, J].cpu()
     bsub = torch.cat([bias[J], bias[n + J]]).cpu()
     dx64, db64, _ = oracle.weighted_bias_bwd(dysub.double(), xsub.double(), bsub.double(), wts.cpu())
     assert_reduction(torch.cat([db[J], db[n + J]]), db64, dx64.abs().sum(0),
                      _bias_depth(rows, n, weighted=True),
-                     "2^32 dbias columns")
+                     "2^32 dbias columns", elem=torch.bfloat16, count=rows)
     del x, dy, dx
     torch.cuda.empty_cache()
 

@@ -91,7 +91,8 @@ def _against_oracle(dy, x, bias, dx, db, what):
     rows, n = dy_c.shape
     assert_parity(dx, oracle.bias_bwd(dy_c, x_c, b_c)[0], f"{what} dx vs oracle")
     dx64, db64 = oracle.bias_bwd(dy_c.double(), x_c.double(), b_c.double())
-    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), f"{what} dbias vs oracle")
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), f"{what} dbias vs oracle",
+                     elem=x.dtype, count=rows)
 
 
 def test_noalloc_refuses_what_does_not_fit(sw):
