@@ -12,9 +12,13 @@
 // to pass through HBM unless the caller asks for it (x_out, the buffer a
 // training step saves).
 //
-// Persistent CTA pairs, one CTA per SM.  Roles (192 threads per CTA): warp 0
-// lane 0 of each CTA TMA-loads that CTA's 128 rows of X and its half of the W
-// slab (64 bf16 of K, 128-byte swizzle) into a 6-stage, 192 KiB ring; warp 1
+// One CTA per SM, in pairs.  The grid holds one cluster per tile, but only as
+// many pairs as fit the SMs start: each takes further tiles by cancelling the
+// launch of clusters that have not started (cluster launch control), so a pair
+// runs until no tile is left, and faster pairs take more tiles.  Roles (192
+// threads per CTA): warp 0 lane 0 of each CTA TMA-loads that CTA's 128 rows
+// of X and its half of the W slab (64 bf16 of K, 128-byte swizzle) into a
+// 6-stage, 192 KiB ring (the leader's also schedules the tiles); warp 1
 // of each CTA takes part in allocating all 512 TMEM columns (two
 // accumulators), and lane 0 of the leader's warp 1 issues
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16, bf16 in, fp32
@@ -52,7 +56,8 @@ static_assert(SWZ_BYTES == 64 || SWZ_BYTES == 128, "64- or 128-byte swizzle");
 constexpr int TMEM_COLS = 2 * UMMA_N;  // two accumulators
 constexpr int kThreads = 192;
 constexpr int kBarrierBytes = 256;
-constexpr int SMEM_BYTES = 192 * 1024 + kBarrierBytes + 1024;  // ring + barriers + alignment slack
+constexpr int RING_BYTES = 192 * 1024;
+constexpr int SMEM_BYTES = RING_BYTES + kBarrierBytes + 1024;  // ring + barriers + alignment slack
 constexpr unsigned long long kTimeoutNs = 2000000000ull;                  // 2 s
 
 __device__ int g_fc1_timeout = 0;
@@ -76,26 +81,41 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// kCluster: acquire at cluster scope, for data another CTA of the cluster
+// wrote before its release arrive on this barrier.
+template <bool kCluster>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if (kCluster)
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n"
+            ".reg .pred p;\n"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "selp.u32 %0, 1, 0, p;\n"
+            "}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Wait for the phase of `bar` with the given parity; false (and the timeout
 // flag raised) if it does not complete within kTimeoutNs.
+template <bool kCluster = false>
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     const uint64_t t0 = now_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait<kCluster>(bar, parity)) {
         if (now_ns() - t0 > kTimeoutNs) {
             atomicExch(&g_fc1_timeout, 1);
             return false;
@@ -155,6 +175,67 @@ __device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_
                  : "memory");
 }
 
+// Two fp32 lanes per instruction (PTX .f32x2 arithmetic, sm_100 and later):
+// each lane rounds to nearest even exactly as the scalar operation does.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// y for 32 accumulator columns of one row: silu(g) * u from the fp32 gate and
+// up dot products, rounded once to bf16, in pairs.  kMayDeep = false when no
+// gate of the chunk is below -64: then each pair takes the streaming kernels'
+// branch-free form, s = 1 / (1 + 2^(-g log2 e)), silu = g s, y = silu u, with
+// the multiplications and the addition done on both lanes at once (the same
+// operations and roundings per element, so the same bits).  The epilogue
+// shares its SM with the tensor pipe, and the fewer FP32 instructions it
+// issues the fewer cycles the pipe loses to it.
+template <bool kMayDeep>
+__device__ __forceinline__ void activate_chunk(const uint32_t (&gv)[32], const uint32_t (&uv)[32],
+                                               uint32_t (&out)[16]) {
+    if constexpr (!kMayDeep) {
+        const uint64_t neg_log2e = f32x2(-swiglu::kLog2e, -swiglu::kLog2e), one = f32x2(1.0f, 1.0f);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const uint64_t g2 = f32x2(__uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
+            const uint64_t u2 = f32x2(__uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
+            float t0, t1, d0, d1, r0, r1;
+            f32x2_split(mul_f32x2(g2, neg_log2e), t0, t1);
+            f32x2_split(add_f32x2(one, f32x2(swiglu::ex2_approx(t0), swiglu::ex2_approx(t1))), d0, d1);
+            const uint64_t s2 = f32x2(swiglu::rcp_approx(d0), swiglu::rcp_approx(d1));
+            f32x2_split(mul_f32x2(mul_f32x2(g2, s2), u2), r0, r1);
+            swiglu::BF16::put2(out, i, r0, r1);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            float r2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float g = __uint_as_float(gv[i + h]);
+                const float u = __uint_as_float(uv[i + h]);
+                const swiglu::Act act = swiglu::activation<swiglu::BF16, false, true>(g);
+                r2[h] = __fmul_rn(__fmul_rn(act.silu, u), act.scale);
+            }
+            swiglu::BF16::put2(out, i, r2[0], r2[1]);
+        }
+    }
+}
+
 // Tile order: groups of kGroupM row tiles; within a group the row tile varies
 // fastest.  A wave of co-resident CTA pairs then covers about kGroupM row tiles
 // x (pairs / kGroupM) column tiles, so its X rows stay in L2 across the whole
@@ -175,8 +256,32 @@ constexpr int kGroupM = 16;
 constexpr int PAIR_M = 2 * BM;
 constexpr int B2_BYTES = BN * BK * 2;                 // this CTA's half of the W slab
 constexpr int STAGE2_BYTES = A_BYTES + B2_BYTES;      // 32 KiB
-constexpr int STAGES2 = (192 * 1024) / STAGE2_BYTES;  // 6
-static_assert(2 * STAGES2 + 7 <= 32, "barriers fit their 256-byte region");
+constexpr int STAGES2 = RING_BYTES / STAGE2_BYTES;     // 6
+static_assert(STAGES2 * STAGE2_BYTES == RING_BYTES, "the ring fills its bytes");
+// Tile scheduling by cluster launch control: the grid has one cluster per
+// tile; a running pair takes further tiles by cancelling the launch of
+// clusters that have not started, so pairs that run faster take more tiles
+// and all finish within about one tile of each other.  The leader's producer
+// thread publishes each tile id in a ring of kTileSlots slots in both CTAs,
+// read by the peer's producer, the MMA thread and the eight epilogue warps.
+constexpr int kTileSlots = 4;
+constexpr int kTileReaders = 1 + 1 + 2 * 4;  // peer producer, MMA thread, epilogue warps
+// the next tile is asked for this many K blocks before the current one's last load
+constexpr int kAskAhead = 16;
+// byte offsets in the region after the ring
+constexpr int OFF_FULL = 0;                                   // full[STAGES2]
+constexpr int OFF_EMPTY = OFF_FULL + 8 * STAGES2;             // empty[STAGES2]
+constexpr int OFF_ACC_FULL = OFF_EMPTY + 8 * STAGES2;         // acc_full[2]
+constexpr int OFF_ACC_EMPTY = OFF_ACC_FULL + 16;              // acc_empty[2]
+constexpr int OFF_MMA_DONE = OFF_ACC_EMPTY + 16;              // mma_done
+constexpr int OFF_TILE_FULL = OFF_MMA_DONE + 8;               // tile_full[kTileSlots]
+constexpr int OFF_TILE_EMPTY = OFF_TILE_FULL + 8 * kTileSlots;  // tile_empty[kTileSlots]
+constexpr int OFF_CLC_BAR = OFF_TILE_EMPTY + 8 * kTileSlots;  // the cancel answer's barrier
+constexpr int OFF_CLC_RESP = (OFF_CLC_BAR + 8 + 15) / 16 * 16;  // the 16-byte answer
+constexpr int OFF_TILE_ID = OFF_CLC_RESP + 16;                // tile_id[kTileSlots]
+constexpr int OFF_TMEM = OFF_TILE_ID + 4 * kTileSlots;        // the TMEM base address
+constexpr int OFF_ABORT = OFF_TMEM + 4;                       // the abort flag
+static_assert(OFF_ABORT + 4 <= kBarrierBytes, "barriers and state fit their region");
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
 // 4-5 = 1), A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 =
 // 0), N / 8 in bits 17-22, M / 16 in bits 24-28 (M = 256 across the pair).
@@ -244,6 +349,47 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
+// Cluster launch control: ask to cancel the launch of a cluster of this grid
+// that has not started; the 16-byte answer is written at `resp` (this CTA's
+// shared memory) and completes 16 bytes of transaction on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            resp),
+        "r"(bar)
+        : "memory");
+}
+
+// The x index of the first CTA of the cluster whose launch was cancelled, or
+// -1 when the request failed (no cluster was left to take).
+__device__ __forceinline__ int clc_cancelled_cta(uint32_t resp) {
+    uint32_t ok, x = 0;
+    asm volatile(
+        "{\n"
+        ".reg .b128 r;\n"
+        ".reg .pred p;\n"
+        "ld.shared.b128 r, [%2];\n"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n"
+        "}\n"
+        : "=r"(ok), "=r"(x)
+        : "r"(resp)
+        : "memory");
+    return ok ? (int)x : -1;
+}
+
+// Write a tile id (-1: none left) into slot `slot` of both CTAs' tile rings
+// and release it with an arrive on each CTA's tile_full barrier.
+__device__ __forceinline__ void publish_tile(uint32_t ids, uint32_t tile_full0, int slot, int tile) {
+#pragma unroll
+    for (uint32_t r = 0; r < 2; ++r) {
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_to_rank(ids + 4 * slot, r)), "r"(tile)
+                     : "memory");
+        mbar_arrive_cluster(map_to_rank(tile_full0 + 8 * slot, r));
+    }
+}
+
 __device__ __forceinline__ void pair_tile_coords(int t, int tiles_m2, int tiles_n, int &m0, int &j0) {
     const int per_group = kGroupM * tiles_n;
     const int g = t / per_group;
@@ -264,13 +410,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     unsigned char *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sa = smem_addr(smem);
     const uint32_t sb = sa + STAGES2 * A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES2 * STAGE2_BYTES);
-    // barriers: full[STAGES2], empty[STAGES2], acc_full[2], acc_empty[2], mma_done
-    const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8 * STAGES2;
-    const uint32_t acc_full0 = empty0 + 8 * STAGES2, acc_empty0 = acc_full0 + 16;
-    const uint32_t mma_done = acc_empty0 + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES2 + 5);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    unsigned char *state = smem + RING_BYTES;
+    const uint32_t st0 = smem_addr(state);
+    const uint32_t full0 = st0 + OFF_FULL, empty0 = st0 + OFF_EMPTY;
+    const uint32_t acc_full0 = st0 + OFF_ACC_FULL, acc_empty0 = st0 + OFF_ACC_EMPTY;
+    const uint32_t mma_done = st0 + OFF_MMA_DONE;
+    const uint32_t tile_full0 = st0 + OFF_TILE_FULL, tile_empty0 = st0 + OFF_TILE_EMPTY;
+    const uint32_t clc_bar = st0 + OFF_CLC_BAR, clc_resp = st0 + OFF_CLC_RESP;
+    const uint32_t tile_ids_addr = st0 + OFF_TILE_ID;
+    volatile int *tile_ids = reinterpret_cast<volatile int *>(state + OFF_TILE_ID);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(state + OFF_TMEM);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(state + OFF_ABORT);
 
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -279,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int tiles_m2 = (M + PAIR_M - 1) / PAIR_M;
     const int tiles_n = (n + BN - 1) / BN;  // the last column tile may be ragged
     const int tiles = tiles_m2 * tiles_n;
-    const int cluster_id = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const uint32_t tile_empty_leader0 = map_to_rank(tile_empty0, 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES2; ++s) {
@@ -291,6 +441,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(acc_empty0 + 8 * a, 8);  // the epilogue warps of both CTAs (leader's copy)
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < kTileSlots; ++i) {
+            mbar_init(tile_full0 + 8 * i, 1);              // the leader's producer
+            mbar_init(tile_empty0 + 8 * i, kTileReaders);  // leader's copy only
+        }
+        mbar_init(clc_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
@@ -311,17 +466,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---- producer (both CTAs): this CTA's X rows and its half of the W slab
-        int it = 0;
-        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters) {
+        // ---- producer (both CTAs): this CTA's X rows and its half of the W
+        // slab for each tile.  The leader's producer also schedules: it
+        // publishes each tile id in both CTAs' tile rings (its own tile
+        // first) and asks for the next by cancelling a pending cluster.
+        // the gate and up halves of W have tensor maps of their own, each n
+        // rows long, so a ragged last column tile reads zeros past row n
+        // instead of rows of the other half
+        const CUtensorMap *wmap = leader ? &tm_wg : &tm_wu;
+        int it = 0, asks = 0;
+        int tile = (int)(blockIdx.x >> 1);
+        for (int k = 0;; ++k) {
+            const int slot = k % kTileSlots;
+            if (leader) {
+                if (!mbar_wait<true>(tile_empty0 + 8 * slot, ((k / kTileSlots) & 1) ^ 1)) {
+                    *abort_flag = 1;
+                    tile = -1;
+                }
+                publish_tile(tile_ids_addr, tile_full0, slot, tile);
+            } else {
+                tile = mbar_wait<true>(tile_full0 + 8 * slot, (k / kTileSlots) & 1) ? tile_ids[slot] : -1;
+                mbar_arrive_cluster(tile_empty_leader0 + 8 * slot);
+            }
+            if (tile < 0) break;
             int m0, j0;
-            pair_tile_coords(t, tiles_m2, tiles_n, m0, j0);
+            pair_tile_coords(tile, tiles_m2, tiles_n, m0, j0);
             const int my_m0 = m0 + BM * (int)rank;
-            // the gate and up halves of W have tensor maps of their own, each
-            // n rows long, so a ragged last column tile reads zeros past row n
-            // instead of rows of the other half
-            const CUtensorMap *wmap = leader ? &tm_wg : &tm_wu;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+            const int ask_at = kblocks > kAskAhead ? kblocks - kAskAhead : 0;
+            bool asked = false;
+            for (int kb = 0; kb < kblocks && !*abort_flag; ++kb, ++it) {
+                if (leader && kb == ask_at) {
+                    mbar_arrive_expect_tx(clc_bar, 16);
+                    clc_try_cancel(clc_resp, clc_bar);
+                    asked = true;
+                }
                 const int s = it % STAGES2;
                 if (!mbar_wait(empty0 + 8 * s, ((it / STAGES2) & 1) ^ 1)) {
                     *abort_flag = 1;
@@ -332,6 +510,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tma_load_2d_pair(sa + s * A_BYTES, &tm_x, full_leader, kb * BK, my_m0);
                 tma_load_2d_pair(sb + s * B2_BYTES, wmap, full_leader, kb * BK, j0);
             }
+            if (leader) {
+                // the answer is waited for even after an abort, so it never
+                // lands in shared memory the CTA has left
+                int next = -1;
+                if (asked && mbar_wait<true>(clc_bar, asks++ & 1)) {
+                    const int x = clc_cancelled_cta(clc_resp);
+                    if (x >= 0) {
+                        next = x >> 1;
+                        if ((x & 1) != 0 || next >= tiles) {  // not a cluster's first CTA of this grid
+                            *abort_flag = 1;
+                            atomicExch(&g_fc1_timeout, 1);
+                            next = -1;
+                        }
+                    }
+                }
+                tile = *abort_flag ? -1 : next;
+            }
         }
         // the leader's full barriers count both CTAs' bytes: once their last
         // phases complete, every load of the pair has landed
@@ -341,7 +536,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && lane == 0 && leader) {
         // ---- MMA issuer (leader only): drives the tensor cores of both SMs
         int it = 0, lt = 0;
-        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters, ++lt) {
+        for (int k = 0;; ++k, ++lt) {
+            const int slot = k % kTileSlots;
+            const int tile = mbar_wait<true>(tile_full0 + 8 * slot, (k / kTileSlots) & 1) ? tile_ids[slot] : -1;
+            mbar_arrive_cluster(tile_empty_leader0 + 8 * slot);
+            if (tile < 0 || *abort_flag) break;
             const int acc = lt & 1;
             if (!mbar_wait(acc_empty0 + 8 * acc, ((lt >> 1) & 1) ^ 1)) {
                 *abort_flag = 1;
@@ -378,13 +577,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const uint32_t acc_empty_leader0 = map_to_rank(acc_empty0, 0);
         int lt = 0;
-        for (int t = cluster_id; t < tiles && !*abort_flag; t += clusters, ++lt) {
+        // the warp leaves the loop as one (its body has warp-wide .sync.aligned
+        // instructions), so the tile id, the abort flag and the waits' outcome
+        // are warp-uniform
+        for (int k = 0;; ++k, ++lt) {
+            const int slot = k % kTileSlots;
+            int tile = -1;
+            if (lane == 0) {
+                if (mbar_wait<true>(tile_full0 + 8 * slot, (k / kTileSlots) & 1)) tile = tile_ids[slot];
+                mbar_arrive_cluster(tile_empty_leader0 + 8 * slot);
+            }
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0 || __shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int acc = lt & 1;
             int m0, j0;
-            pair_tile_coords(t, tiles_m2, tiles_n, m0, j0);
+            pair_tile_coords(tile, tiles_m2, tiles_n, m0, j0);
             const int row = m0 + BM * (int)rank + 32 * quarter + lane;
-            if (!mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1)) {
-                *abort_flag = 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(acc_full0 + 8 * acc, (lt >> 1) & 1))) {
+                if (lane == 0) *abort_flag = 1;
                 break;
             }
             tc_fence_after();
@@ -402,18 +612,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (row < M) {
                     uint32_t out[16];
+                    // gates below -64 need the scaled deep-tail form; a chunk
+                    // without any takes the branch-free form (the same bits
+                    // per element) with a much shorter instruction stream
+                    float gmin = __uint_as_float(gv[0]);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        float r2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float g = __uint_as_float(gv[i + h]);
-                            const float u = __uint_as_float(uv[i + h]);
-                            const swiglu::Act act = swiglu::activation<swiglu::BF16, false>(g);
-                            r2[h] = __fmul_rn(__fmul_rn(act.silu, u), act.scale);
-                        }
-                        swiglu::BF16::put2(out, i, r2[0], r2[1]);
-                    }
+                    for (int i = 1; i < 32; ++i) gmin = fminf(gmin, __uint_as_float(gv[i]));
+                    if (!(gmin < -64.0f))
+                        activate_chunk<false>(gv, uv, out);
+                    else
+                        activate_chunk<true>(gv, uv, out);
                     __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -527,9 +735,8 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     if (!make_map(enc, &tm_x, x_in, M, K) || !make_map(enc, &tm_wg, w, n, K) ||
         !make_map(enc, &tm_wu, w_up, n, K))
         return fail(cudaErrorInvalidValue);
-    int dev = 0, sms = 0;
+    int dev = 0;
     e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
     // the shared-memory opt-in is a per-device function attribute
     constexpr int kMaxDevices = 64;
@@ -542,9 +749,10 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
         if (dev >= 0 && dev < kMaxDevices) attr_set[dev].store(true);
     }
     const int64_t tiles = ((M + PAIR_M - 1) / PAIR_M) * ((n + BN - 1) / BN);  // 256 x 128 tiles
-    if (tiles > INT32_MAX) return SWIGLU_ERR_SHAPE;
-    const int64_t pairs = tiles < sms / 2 ? tiles : sms / 2;
-    const dim3 grid((unsigned)(2 * (pairs > 0 ? pairs : 1)));
+    if (tiles > INT32_MAX / 2) return SWIGLU_ERR_SHAPE;
+    // one cluster per tile; the pairs that start take the others' tiles
+    // (cluster launch control), so only as many run as fit on the SMs
+    const dim3 grid((unsigned)(2 * tiles));
     fc1_swiglu_pair_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
         tm_x, tm_wg, tm_wu, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
         (int)n, (int)K);
