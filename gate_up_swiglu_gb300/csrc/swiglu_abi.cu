@@ -500,17 +500,16 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
         bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    constexpr int RT = swiglu::kReduceThreads;
-    int64_t rgrid = (2 * a.n + RT - 1) / RT;
-    if (rgrid > (int64_t)d.sms * 16) rgrid = (int64_t)d.sms * 16;
-    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)rgrid, RT, 0, stream>>>(a.partial, b.groups,
-                                                                              2 * a.n, a.dbias);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || !WEIGHTED) return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
-    int64_t wgrid = (a.rows + RT - 1) / RT;
-    if (wgrid > (int64_t)d.sms * 16) wgrid = (int64_t)d.sms * 16;
-    swiglu::swiglu_dw_reduce_kernel<<<(unsigned)wgrid, RT, 0, stream>>>(a.partial_dw, a.rows,
-                                                                        (int32_t)b.tiles, a.dw);
+    // the reductions: kReduceCols columns of dbias per CTA, then (with
+    // weights) kReduceThreads rows of dw per CTA, in one launch
+    constexpr int64_t RC = swiglu::kReduceCols, RT = swiglu::kReduceThreads, kCap = 8;
+    int64_t col_ctas = (2 * a.n + RC - 1) / RC;
+    if (col_ctas > (int64_t)d.sms * kCap) col_ctas = (int64_t)d.sms * kCap;
+    int64_t dw_ctas = WEIGHTED ? (a.rows + RT - 1) / RT : 0;
+    if (dw_ctas > (int64_t)d.sms * kCap) dw_ctas = (int64_t)d.sms * kCap;
+    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)(col_ctas + dw_ctas), (unsigned)RT, 0, stream>>>(
+        a.partial, b.groups, 2 * a.n, a.dbias, col_ctas, a.partial_dw, WEIGHTED ? a.rows : 0,
+        (int32_t)b.tiles, a.dw);
     e = cudaGetLastError();
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }

@@ -1049,11 +1049,23 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 
 // Threads per CTA of the two reduction passes below (small CTAs: the grids
 // have one thread per column or row, fewer than the SMs hold).
-constexpr int kReduceThreads = 128;
+// Bias backward, second pass.  dbias[k] = the sum over row groups of
+// partial[group][k], rounded once to the storage type: a CTA takes
+// kReduceCols consecutive columns (one per lane, so each group's row is one
+// coalesced load per warp), its kReduceSegs warps sum contiguous segments of
+// the groups in group order, and warp 0 adds the segment sums in segment
+// order -- a fixed tree, so the result does not depend on timing, and the
+// chain behind each value is about groups / kReduceSegs + kReduceSegs long
+// instead of `groups`.  With dw (the weights + bias form), the CTAs after the
+// column CTAs also form dw[r] = the sum over column tiles of partial_dw[r][tile],
+// in tile order, so both reductions take one launch.
+constexpr int kReduceCols = 32;
+constexpr int kReduceSegs = 8;
+constexpr int kReduceThreads = kReduceCols * kReduceSegs;
 
 // Sum of the `count` floats at p, p + stride, ..., added in that order; the
-// loads go out eight at a time so a long chain of groups does not wait on
-// one load latency per term.
+// loads go out eight at a time so a long chain does not wait on one load
+// latency per term.
 __device__ __forceinline__ float ordered_sum(const float *p, int64_t count, int64_t stride) {
     float s = 0.0f;
     int64_t q = 0;
@@ -1068,31 +1080,39 @@ __device__ __forceinline__ float ordered_sum(const float *p, int64_t count, int6
     return s;
 }
 
-// Bias backward, second pass: dbias[k] = sum over groups of partial[group][k],
-// in group order, rounded once to the storage type.
 template <typename E>
-__global__ void __launch_bounds__(kReduceThreads) swiglu_bias_reduce_kernel(const float *partial,
-                                                                            int64_t groups,
-                                                                            int64_t two_n,
-                                                                            void *dbias) {
-    for (int64_t k = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; k < two_n;
-         k += (int64_t)gridDim.x * kReduceThreads) {
-        const float s = ordered_sum(partial + k, groups, two_n);
-        uint32_t w[1] = {0};
-        E::put(w, 0, s);
-        if (E::kBytes == 4)
-            static_cast<uint32_t *>(dbias)[k] = w[0];
-        else
-            static_cast<unsigned short *>(dbias)[k] = (unsigned short)w[0];
+__global__ void __launch_bounds__(kReduceThreads)
+    swiglu_bias_reduce_kernel(const float *partial, int64_t groups, int64_t two_n, void *dbias,
+                              int64_t col_ctas, const float *partial_dw, int64_t rows, int32_t tiles,
+                              float *dw) {
+    if ((int64_t)blockIdx.x >= col_ctas) {  // dw rows (whole CTAs, so no barrier diverges)
+        for (int64_t r = ((int64_t)blockIdx.x - col_ctas) * kReduceThreads + threadIdx.x; r < rows;
+             r += ((int64_t)gridDim.x - col_ctas) * kReduceThreads)
+            dw[r] = ordered_sum(partial_dw + r * tiles, tiles, 1);
+        return;
     }
-}
-
-// dw[r] = sum over column tiles of partial_dw[r, tile], in tile order.
-static __global__ void __launch_bounds__(kReduceThreads)
-    swiglu_dw_reduce_kernel(const float *partial_dw, int64_t rows, int32_t tiles, float *dw) {
-    for (int64_t r = (int64_t)blockIdx.x * kReduceThreads + threadIdx.x; r < rows;
-         r += (int64_t)gridDim.x * kReduceThreads)
-        dw[r] = ordered_sum(partial_dw + r * tiles, tiles, 1);
+    __shared__ float seg[kReduceSegs][kReduceCols];
+    const int lane = threadIdx.x % kReduceCols, warp = threadIdx.x / kReduceCols;
+    const int64_t per = (groups + kReduceSegs - 1) / kReduceSegs;
+    const int64_t g0 = warp * per;
+    const int64_t cnt = g0 < groups ? (groups - g0 < per ? groups - g0 : per) : 0;
+    for (int64_t c0 = (int64_t)blockIdx.x * kReduceCols; c0 < two_n; c0 += col_ctas * kReduceCols) {
+        const int64_t k = c0 + lane;
+        seg[warp][lane] = k < two_n ? ordered_sum(partial + g0 * two_n + k, cnt, two_n) : 0.0f;
+        __syncthreads();
+        if (warp == 0 && k < two_n) {
+            float t = seg[0][lane];
+#pragma unroll
+            for (int w = 1; w < kReduceSegs; ++w) t = __fadd_rn(t, seg[w][lane]);
+            uint32_t word[1] = {0};
+            E::put(word, 0, t);
+            if (E::kBytes == 4)
+                static_cast<uint32_t *>(dbias)[k] = word[0];
+            else
+                static_cast<unsigned short *>(dbias)[k] = (unsigned short)word[0];
+        }
+        __syncthreads();
+    }
 }
 
 }  // namespace swiglu

@@ -77,15 +77,16 @@ def assert_reduction(gpu, exact, abs_sum, depth, what, *, elem, count):
 
 
 def _bias_depth(rows, n, weighted=False):
-    """Chained additions behind one dbias value: the rows of one row group,
-    then the row groups.  The plan fills every SM once with 2 (bias) or 3
-    (weights + bias) tile CTAs."""
+    """Chained additions behind one dbias value: the rows of one row group
+    (the tile kernel), then one of 8 contiguous segments of the row groups,
+    then the 8 segment sums (the reduce kernel).  The plan fills every SM once
+    with 2 (bias) or 3 (weights + bias) tile CTAs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tiles = -(-n // 2048)
     groups = max(1, min(rows, (sms * (3 if weighted else 2)) // tiles))
     rpg = -(-rows // groups)
     groups = -(-rows // rpg)
-    return rpg + groups
+    return rpg + -(-groups // 8) + 8
 
 
 CASES = [("tiny_f32", None), ("megatron_4096_bf16", 300), ("odd_5503_f32", 97),
