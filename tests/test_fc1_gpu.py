@@ -135,7 +135,8 @@ def test_fc1_module_gradients(sw, in_place):
     assert sw.fc1_timeout_flag() == 0
 
 
-@pytest.mark.parametrize("M,n,K", [(256, 256, 512), (300, 384, 136), (257, 200, 64)])
+@pytest.mark.parametrize("M,n,K", [(256, 256, 512), (300, 384, 136), (257, 200, 64),
+                                   (2048, 2560, 136)])
 def test_fc1_exact_on_integer_inputs(sw, M, n, K):
     """Integer X, W in [-3, 3]: every product and partial sum is an integer
     below 2^24, so the tensor cores' fp32 accumulation is exact whatever its
@@ -151,3 +152,30 @@ def test_fc1_exact_on_integer_inputs(sw, M, n, K):
     assert torch.equal(fc1.cpu().view(torch.int16), fc1_or.view(torch.int16))
     d = (bf16_ordered(y.cpu()) - bf16_ordered(y_or)).abs()
     assert int(d.max()) <= 1
+
+
+def test_fc1_tiles_taken_beside_another_stream(sw):
+    """More tiles than CTA pairs fit (the running pairs take the rest by
+    cancelling pending launches), with a streaming workload holding SMs on a
+    second stream at the same time: y is bit for bit that of fc1 run alone,
+    and no wait gave up."""
+    M, K, n = 2048, 1024, 4096  # 8 x 32 = 256 tiles of 256 x 128
+    g = torch.Generator(device="cuda").manual_seed(11)
+    X = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    Wt = (torch.randn(2 * n, K, generator=g, device="cuda") / K ** 0.5).to(torch.bfloat16)
+    y0 = sw.swiglu_fc1_fwd(X, Wt)
+    torch.cuda.synchronize()
+    x_big = torch.randn(8192, 2 * 16384, generator=g, device="cuda").to(torch.bfloat16)
+    dy_big = torch.randn(8192, 16384, generator=g, device="cuda").to(torch.bfloat16)
+    other = torch.cuda.Stream()
+    ys = []
+    for _ in range(3):
+        with torch.cuda.stream(other):
+            for _ in range(4):
+                sw.swiglu_gateup_bwd(dy_big, x_big)
+        ys.append(sw.swiglu_fc1_fwd(X, Wt))
+    torch.cuda.synchronize()
+    assert sw.fc1_timeout_flag() == 0
+    for y in ys:
+        assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
