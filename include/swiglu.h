@@ -271,13 +271,18 @@ swiglu_status_t swiglu_gateup_bias_bwd_noalloc(const void *dy, const void *x, co
  *                 rows [n, 2n) up), contiguous         (read)
  *   y     [M, n]  bf16, contiguous                     (written)
  *   x_out [M, 2n] bf16, contiguous, or NULL            (written)
- * Requirements: n and K multiples of 8, K >= 8, M, K, 2n below 2^31 (else
+ * Requirements: n and K multiples of 8, K >= 8, M, K, 2n below 2^31 and
+ * ceil(M / 256) * ceil(n / 128) (the tile count) below 2^30 (else
  * SWIGLU_ERR_SHAPE); all pointers 16-byte aligned
  * (else SWIGLU_ERR_STRIDE); outputs overlap no input and each other
  * (SWIGLU_ERR_ALIAS); dtype SWIGLU_BF16 (else SWIGLU_ERR_DTYPE).  M == 0 or
- * n == 0 is an empty call.  Each CTA bounds its internal waits; a wait that
- * times out raises the flag read by swiglu_fc1_timeout_flag (results of that
- * call are then undefined).
+ * n == 0 is an empty call.  The launch holds one 2-CTA cluster per tile; the
+ * pairs that fit run and take the other tiles by cancelling launches that
+ * have not started, so the result does not depend on how many SMs other
+ * streams' work leaves free.  Each CTA bounds its internal waits; a wait that
+ * times out, or a cancellation answer that names no tile of the grid, raises
+ * the flag read by swiglu_fc1_timeout_flag (results of that call are then
+ * undefined).
  */
 swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x_out, int64_t M,
                                int64_t n, int64_t K, swiglu_dtype_t dtype, swiglu_stream_t stream);
