@@ -835,18 +835,20 @@ def l2_note(w: W.Workload) -> str:
     return f"inputs {inputs / 2**20:.0f} MiB fit in L2 {l2 / 2**20:.0f} MiB: L2-resident timing"
 
 
-def link_rates(dev, h_in: torch.Tensor, h_out: torch.Tensor) -> dict:
-    """Host link rates of the given page-locked buffers, same run: h_in copied
-    to the device alone, the device copied into h_out alone, then both at once
-    on two streams (GB/s each way, best of 3).  The duplex rate depends on
-    where the buffers land in host memory (149-170 GB/s on one box across
-    buffer sets), so it is measured on the very buffers the end-to-end step
-    uses."""
-    nbytes = min(h_in.numel() * h_in.element_size(), h_out.numel() * h_out.element_size())
-    src = h_in.view(-1).view(torch.uint8)[:nbytes]
-    dst = h_out.view(-1).view(torch.uint8)[:nbytes]
-    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+def link_rates(dev, h_ins, h_outs) -> dict:
+    """Host link rates of the given page-locked buffers, same run: every h_in
+    copied to the device alone, the device copied into every h_out alone, then
+    both directions at once on two streams (GB/s each way, best of 3).  The
+    rates depend on where the buffers land in host memory (149-170 GB/s duplex
+    on one box across buffer sets), so they are measured on the very buffers
+    the end-to-end step uses, all of them."""
+    def flat(ts):
+        return [t.view(-1).view(torch.uint8) for t in ts]
+
+    srcs, dsts = flat(h_ins), flat(h_outs)
+    b_in, b_out = sum(t.numel() for t in srcs), sum(t.numel() for t in dsts)
+    d_in = [torch.empty(t.numel(), dtype=torch.uint8, device=dev) for t in srcs]
+    d_out = [torch.empty(t.numel(), dtype=torch.uint8, device=dev) for t in dsts]
     s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def best(fn):
@@ -859,19 +861,26 @@ def link_rates(dev, h_in: torch.Tensor, h_out: torch.Tensor) -> dict:
             ts.append(time.perf_counter() - t)
         return min(ts)
 
+    def copy_in():
+        for d, h in zip(d_in, srcs):
+            d.copy_(h, non_blocking=True)
+
+    def copy_out():
+        for h, d in zip(dsts, d_out):
+            h.copy_(d, non_blocking=True)
+
     def both():
         with torch.cuda.stream(s1):
-            d_in.copy_(src, non_blocking=True)
+            copy_in()
         with torch.cuda.stream(s2):
-            dst.copy_(d_out, non_blocking=True)
+            copy_out()
 
-    t_in = best(lambda: d_in.copy_(src, non_blocking=True))
-    t_out = best(lambda: dst.copy_(d_out, non_blocking=True))
-    t_both = best(both)
-    return {"h2d_gbs": round(nbytes / t_in / 1e9, 1), "d2h_gbs": round(nbytes / t_out / 1e9, 1),
-            "duplex_each_way_gbs": round(nbytes / t_both / 1e9, 1),
-            "copy_bytes": nbytes,
-            "how": "the step's own pinned x (in) and dx (out) buffers, host clock, best of 3"}
+    t_in, t_out, t_both = best(copy_in), best(copy_out), best(both)
+    # both at once: each direction's rate over the time both took
+    return {"h2d_gbs": round(b_in / t_in / 1e9, 1), "d2h_gbs": round(b_out / t_out / 1e9, 1),
+            "duplex_each_way_gbs": round(max(b_in, b_out) / t_both / 1e9, 1),
+            "h2d_bytes": b_in, "d2h_bytes": b_out,
+            "how": "the step's own pinned buffers (x, dy in; y, dx out), host clock, best of 3"}
 
 
 def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
@@ -910,7 +919,7 @@ def end_to_end(sw, w, x_dev, dy_dev, dev, K, barrier, reduce):
     h2d = xh.numel() * xh.element_size() + dyh.numel() * dyh.element_size()
     d2h = yh.numel() * yh.element_size() + dxh.numel() * dxh.element_size()
     del staging
-    link = link_rates(dev, xh, dxh)
+    link = link_rates(dev, (xh, dyh), (yh, dxh))
     del xh, dyh, yh, dxh
     # the floor set by the link: the larger direction at the measured duplex rate
     floor_ms = max(h2d, d2h) / (link["duplex_each_way_gbs"] * 1e9) * 1e3

@@ -18,6 +18,27 @@
 
 namespace {
 
+// Launch with programmatic stream serialization (pdl): the kernel may launch
+// while the previous kernel in the stream finishes; it waits for that
+// kernel's completion itself (await_previous_grid, at the top of every kernel
+// here).  pdl = false launches it after the previous kernel, as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+
 constexpr int kMaxDevices = 64;
 thread_local int g_last_cuda_error = 0;
 
@@ -303,8 +324,7 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     p.div_nvec = make_fast_div((uint64_t)nvec);
     p.nvec = (int32_t)nvec;
     p.step_r = (int32_t)(step % nvec);
-    kernel<<<(unsigned)grid, T, 0, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(true, kernel, (unsigned)grid, T, 0, stream, p);
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
@@ -374,8 +394,7 @@ swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t row
     p.segments = segments;
     p.div_chunks = make_fast_div((uint64_t)chunks);
     p.chunks = (int32_t)chunks;
-    kernel<<<(unsigned)grid, Sh::T, 0, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(true, kernel, (unsigned)grid, Sh::T, 0, stream, p);
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
@@ -435,8 +454,7 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     swiglu::BwdParams p = bwd_params(a, VEC);
     p.step_q = step / nvec;
     p.step_r = (int32_t)(step % nvec);
-    kernel<<<(unsigned)grid, T, 0, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_pdl(true, kernel, (unsigned)grid, T, 0, stream, p);
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
@@ -454,11 +472,13 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
     static_assert(ctas_cap(kRowPolicy, E::kBytes * VEC) > 0, "the row kernel is persistent");
+    const int fit = per_sm;
     if (per_sm > ctas_cap(kRowPolicy, E::kBytes * VEC)) per_sm = ctas_cap(kRowPolicy, E::kBytes * VEC);
     int64_t grid = (int64_t)d.sms * per_sm;
     if (grid > a.rows) grid = a.rows;
-    kernel<<<(unsigned)grid, swiglu::kThreads, 0, stream>>>(bwd_params(a, VEC));
-    e = cudaGetLastError();
+    // a fixed number of row-walking CTAs per SM, as in the bias tile kernel:
+    // launched early only when that fills every SM (below that, 4.5 % slower)
+    e = launch_pdl(per_sm >= fit, kernel, (unsigned)grid, swiglu::kThreads, 0, stream, bwd_params(a, VEC));
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
@@ -496,9 +516,18 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
         }
     }
     const BiasPlan b = bias_plan(a.rows, a.n, d.sms, WEIGHTED);
-    kernel<<<(unsigned)(b.tiles * b.groups), swiglu::kThreads, ring, stream>>>(
-        bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
-    e = cudaGetLastError();
+    // The plan is one wave of a fixed number of CTAs per SM, each walking its
+    // rows, and the SM's issue bounds them: launched early beside the previous
+    // grid's last CTAs, an SM may take one CTA more than the plan and another
+    // one less (bias form, large FFN: 7 % slower).  So it launches early only
+    // when the plan fills every SM.
+    static std::atomic<int> occ[kMaxDevices];
+    int fit = 0;
+    e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, fit, (size_t)ring);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int planned = WEIGHTED ? kWeightedBiasCtasPerSm : kBiasCtasPerSm;
+    e = launch_pdl(planned >= fit, kernel, (unsigned)(b.tiles * b.groups), swiglu::kThreads, (size_t)ring, stream,
+                   bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     if (e != cudaSuccess) return cuda_fail(e);
     // the reductions: kReduceCols columns of dbias per CTA, then (with
     // weights) kReduceThreads rows of dw per CTA, in one launch
@@ -507,10 +536,9 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     if (col_ctas > (int64_t)d.sms * kCap) col_ctas = (int64_t)d.sms * kCap;
     int64_t dw_ctas = WEIGHTED ? (a.rows + RT - 1) / RT : 0;
     if (dw_ctas > (int64_t)d.sms * kCap) dw_ctas = (int64_t)d.sms * kCap;
-    swiglu::swiglu_bias_reduce_kernel<E><<<(unsigned)(col_ctas + dw_ctas), (unsigned)RT, 0, stream>>>(
-        a.partial, b.groups, 2 * a.n, a.dbias, col_ctas, a.partial_dw, WEIGHTED ? a.rows : 0,
-        (int32_t)b.tiles, a.dw);
-    e = cudaGetLastError();
+    e = launch_pdl(true, swiglu::swiglu_bias_reduce_kernel<E>, (unsigned)(col_ctas + dw_ctas), (unsigned)RT, 0,
+                   stream, a.partial, b.groups, 2 * a.n, a.dbias, col_ctas, a.partial_dw,
+                   WEIGHTED ? a.rows : 0, (int32_t)b.tiles, a.dw);
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 

@@ -224,6 +224,21 @@ struct BF16 {
     }
 };
 
+// ------------------------------------------- programmatic dependent launch ---
+// The host launches every streaming kernel so that the next kernel in the
+// stream may launch while this one's last CTAs still run (sm_90 and later).
+// Each kernel therefore first waits until the grid before it in the stream has
+// completed and its writes are visible -- before any global memory access,
+// read or write -- and later lets the next one launch: once every CTA of a
+// grid has done so, the next grid's CTAs are placed on SMs as room appears and
+// start the moment this grid completes, instead of after a full launch.
+// Every kernel lets it go at the top: for a grid of many waves that happens
+// once its last wave has started.
+__device__ __forceinline__ void await_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ math ---
 // fp32 (and the deep bf16 tail): sigmoid(g) and 1 - sigmoid(g) come from
 // t = exp(-|g|) in (0, 1]:
@@ -496,6 +511,8 @@ __device__ __forceinline__ void fwd_pack(const uint32_t *g, const uint32_t *u, c
 template <typename E, int VEC, int U, int LD, int ST, int MODE = kPlain, int T = kThreads,
           bool SPLIT = true>
 __global__ void __launch_bounds__(T, MODE == kBiasWeight ? 4 : 0) swiglu_fwd_kernel(const FwdParams p) {
+    await_previous_grid();
+    allow_next_grid();
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     using L = Ld<B, LD>;
@@ -572,6 +589,8 @@ __device__ __forceinline__ void bwd_pack(const uint32_t *d, const uint32_t *g, c
 // arithmetic is the same template body, so both instances give identical bits.
 template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST, int T = kThreads>
 __global__ void __launch_bounds__(T) swiglu_bwd_kernel(const BwdParams p) {
+    await_previous_grid();
+    allow_next_grid();
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256),
                   "the in-place backward writes what it reads: no read-only loads");
     constexpr int B = E::kBytes * VEC;
@@ -650,6 +669,8 @@ struct SegParams {
 // backward is the plain form only.
 template <typename E, int MODE, int K, int T, int LD, int FMODE = kPlain>
 __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
+    await_previous_grid();
+    allow_next_grid();
     constexpr int EB = E::kBytes;
     constexpr int NIN = MODE == kSegFwd ? 2 : 3;
     constexpr int NOUT = MODE == kSegFwd ? 1 : 2;
@@ -781,6 +802,8 @@ __device__ __forceinline__ void weighted_pack(const uint32_t *d, const uint32_t 
 
 template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
 __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const BwdParams p) {
+    await_previous_grid();
+    allow_next_grid();
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
@@ -878,6 +901,8 @@ template <typename E, int VEC, bool IN_PLACE, int LD, int ST, bool WEIGHTED = fa
           int DW_BATCH = 32>
 __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
                                                                       int64_t rows_per_group) {
+    await_previous_grid();
+    allow_next_grid();
     constexpr int MODE = WEIGHTED ? kBiasWeight : kBias;
     constexpr int kDwBatch = DW_BATCH;
     __shared__ float wpart[WEIGHTED ? kDwBatch : 1][WEIGHTED ? kThreads : 1];
@@ -1047,8 +1072,6 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     }
 }
 
-// Threads per CTA of the two reduction passes below (small CTAs: the grids
-// have one thread per column or row, fewer than the SMs hold).
 // Bias backward, second pass.  dbias[k] = the sum over row groups of
 // partial[group][k], rounded once to the storage type: a CTA takes
 // kReduceCols consecutive columns (one per lane, so each group's row is one
@@ -1085,6 +1108,8 @@ __global__ void __launch_bounds__(kReduceThreads)
     swiglu_bias_reduce_kernel(const float *partial, int64_t groups, int64_t two_n, void *dbias,
                               int64_t col_ctas, const float *partial_dw, int64_t rows, int32_t tiles,
                               float *dw) {
+    await_previous_grid();
+    allow_next_grid();
     if ((int64_t)blockIdx.x >= col_ctas) {  // dw rows (whole CTAs, so no barrier diverges)
         for (int64_t r = ((int64_t)blockIdx.x - col_ctas) * kReduceThreads + threadIdx.x; r < rows;
              r += ((int64_t)gridDim.x - col_ctas) * kReduceThreads)
