@@ -464,6 +464,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched early (programmatic dependent launch): the setup above ran
+    // beside the previous grid's last CTAs; from here on every role may touch
+    // global memory, so wait until that grid has completed and its writes are
+    // visible.  The next grid may launch now: its CTAs take SMs as this
+    // grid's pairs leave.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 && lane == 0) {
         // ---- producer (both CTAs): this CTA's X rows and its half of the W
@@ -753,10 +760,21 @@ swiglu_status_t swiglu_fc1_fwd(const void *x_in, const void *w, void *y, void *x
     // one cluster per tile; the pairs that start take the others' tiles
     // (cluster launch control), so only as many run as fit on the SMs
     const dim3 grid((unsigned)(2 * tiles));
-    fc1_swiglu_pair_kernel<<<grid, kThreads, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tm_x, tm_wg, tm_wu, static_cast<__nv_bfloat16 *>(y), static_cast<__nv_bfloat16 *>(x_out), (int)M,
-        (int)n, (int)K);
-    e = cudaGetLastError();
+    // programmatic stream serialization: the grid may launch while the
+    // previous kernel in the stream finishes (the kernel waits for it before
+    // its first global memory access)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fc1_swiglu_pair_kernel, tm_x, tm_wg, tm_wu, static_cast<__nv_bfloat16 *>(y),
+                           static_cast<__nv_bfloat16 *>(x_out), (int)M, (int)n, (int)K);
     return e == cudaSuccess ? SWIGLU_OK : fail(e);
 }
 
