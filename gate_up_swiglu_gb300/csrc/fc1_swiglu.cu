@@ -174,6 +174,28 @@ __device__ __forceinline__ void store16(void *p, uint32_t a, uint32_t b, uint32_
                  "r"(d)
                  : "memory");
 }
+// 32 bytes (sm_100-class 256-bit store): a whole sector
+__device__ __forceinline__ void store32(void *p, const uint32_t *w) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// The 16 words of 32 output columns of one row, from column `col` on (n % 8
+// == 0, so a 16-byte piece is all inside or all outside the row): as two
+// 32-byte stores when `wide` (rows and base 32-byte aligned), else four.
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *p, const uint32_t (&w)[16], int col, int n,
+                                                bool wide) {
+    if (wide) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (col + 16 * q < n) store32(p + 16 * q, w + 8 * q);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (col + 8 * q < n) store16(p + 8 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+}
 
 // Two fp32 lanes per instruction (PTX .f32x2 arithmetic, sm_100 and later):
 // each lane rounds to nearest even exactly as the scalar operation does.
@@ -583,6 +605,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ---- epilogue (both CTAs): this CTA's 128 rows of the accumulator
         const int quarter = warp & 3;
         const uint32_t acc_empty_leader0 = map_to_rank(acc_empty0, 0);
+        // 32-byte stores when every output row starts on a 32-byte boundary
+        const bool wide = n % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 32 == 0 &&
+                          reinterpret_cast<uintptr_t>(x_out) % 32 == 0;
         int lt = 0;
         // the warp leaves the loop as one (its body has warp-wide .sync.aligned
         // instructions), so the tile id, the abort flag and the waits' outcome
@@ -629,11 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         activate_chunk<false>(gv, uv, out);
                     else
                         activate_chunk<true>(gv, uv, out);
-                    __nv_bfloat16 *yr = y + (int64_t)row * n + j0 + c;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (j0 + c + 8 * q < n)  // n % 8 == 0: a 16-byte store is all in or all out
-                            store16(yr + 8 * q, out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                    store_row_chunk(y + (int64_t)row * n + j0 + c, out, j0 + c, n, wide);
                     if (x_out != nullptr) {
                         uint32_t pg[16], pu[16];
 #pragma unroll
@@ -642,14 +663,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             swiglu::BF16::put2(pu, i, __uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
                         }
                         __nv_bfloat16 *xg = x_out + (int64_t)row * 2 * n + j0 + c;
-                        __nv_bfloat16 *xu = xg + n;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (j0 + c + 8 * q < n) {
-                                store16(xg + 8 * q, pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-                                store16(xu + 8 * q, pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
-                            }
-                        }
+                        store_row_chunk(xg, pg, j0 + c, n, wide);
+                        store_row_chunk(xg + n, pu, j0 + c, n, wide);
                     }
                 }
             }
