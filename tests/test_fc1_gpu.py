@@ -154,6 +154,34 @@ def test_fc1_exact_on_integer_inputs(sw, M, n, K):
     assert int(d.max()) <= 1
 
 
+def _random_fc1_shape(i):
+    g = torch.Generator().manual_seed(700 + i)
+    pick = lambda lo, hi: int(torch.randint(lo, hi + 1, (1,), generator=g))  # noqa: E731
+    return pick(1, 700), 8 * pick(1, 90), 8 * pick(1, 40)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_fc1_random_shapes_exact(sw, i):
+    """Seeded random M, n (a multiple of 8) and K (a multiple of 8): ragged row
+    and column tiles and K blocks of every kind.  Integer inputs in [-3, 3]
+    make the fp32 accumulation exact, so the stored fc1 equals the oracle's
+    once-rounded exact value bit for bit and y is within one bf16 step."""
+    M, n, K = _random_fc1_shape(i)
+    g = torch.Generator().manual_seed(900 + i)
+    X = torch.randint(-3, 4, (M, K), generator=g).to(torch.bfloat16)
+    Wt = torch.randint(-3, 4, (2 * n, K), generator=g).to(torch.bfloat16)
+    y, fc1 = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda(), return_fc1=True)
+    y_only = sw.swiglu_fc1_fwd(X.cuda(), Wt.cuda())
+    torch.cuda.synchronize()
+    assert sw.fc1_timeout_flag() == 0
+    y_or, fc1_or = oracle.fc1_swiglu_fwd(X, Wt, want_fc1=True)
+    what = f"M {M} n {n} K {K}"
+    assert torch.equal(fc1.cpu().view(torch.int16), fc1_or.view(torch.int16)), what
+    d = (bf16_ordered(y.cpu()) - bf16_ordered(y_or)).abs()
+    assert int(d.max()) <= 1, what
+    assert torch.equal(y_only.view(torch.int16), y.view(torch.int16)), what
+
+
 def test_fc1_tiles_taken_beside_another_stream(sw):
     """More tiles than CTA pairs fit (the running pairs take the rest by
     cancelling pending launches), with a streaming workload holding SMs on a
