@@ -950,6 +950,13 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
         for (int i = 0; i < VEC; ++i) ag[k][i] = au[k][i] = 0.0f;
     }
+    // Byte address of pack k of row r of an operand: one multiply-add per row
+    // and operand (r * stride + c[0]), then a constant offset per k (c[k] =
+    // c[0] + k * kThreads), which the loads and stores take as an immediate.
+    const int64_t c0 = c[0];
+    auto at = [&](const void *base, int64_t stride, int64_t r, int k) -> const char * {
+        return static_cast<const char *>(base) + (r * stride + c0) * B + (int64_t)k * kThreads * B;
+    };
     // ring slot of (stage, operand, pack) for this thread
     auto ring_at = [&](int st, int x, int k) -> unsigned char * {
         return bias_ring + ((size_t)((st * 3 + x) * PPT + k) * kThreads + threadIdx.x) * B;
@@ -960,9 +967,9 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
             for (int k = 0; k < PPT; ++k) {
                 if (c[k] < p.nvec) {
-                    cp_async_pack<B>(ring_at(st, 0, k), static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B);
-                    cp_async_pack<B>(ring_at(st, 1, k), static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B);
-                    cp_async_pack<B>(ring_at(st, 2, k), static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B);
+                    cp_async_pack<B>(ring_at(st, 0, k), at(p.dy, p.dy_stride, r, k));
+                    cp_async_pack<B>(ring_at(st, 1, k), at(p.g, p.g_stride, r, k));
+                    cp_async_pack<B>(ring_at(st, 2, k), at(p.u, p.u_stride, r, k));
                 }
             }
         }
@@ -1016,9 +1023,9 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
 #pragma unroll
                 for (int k = 0; k < PPT; ++k) {
                     if (r < r1 && c[k] < p.nvec) {
-                        L::run(static_cast<const char *>(p.dy) + (r * p.dy_stride + c[k]) * B, d[q][k]);
-                        L::run(static_cast<const char *>(p.g) + (r * p.g_stride + c[k]) * B, g[q][k]);
-                        L::run(static_cast<const char *>(p.u) + (r * p.u_stride + c[k]) * B, u[q][k]);
+                        L::run(at(p.dy, p.dy_stride, r, k), d[q][k]);
+                        L::run(at(p.g, p.g_stride, r, k), g[q][k]);
+                        L::run(at(p.u, p.u_stride, r, k), u[q][k]);
                     }
                 }
             }
@@ -1041,8 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
                                                        ag[k], au[k], rowsum, gv, uv);
                     store_pack<E, VEC>(og, gv);
                     store_pack<E, VEC>(ou, uv);
-                    S::run(static_cast<char *>(p.dg) + (r * p.dg_stride + c[k]) * B, og);
-                    S::run(static_cast<char *>(p.du) + (r * p.du_stride + c[k]) * B, ou);
+                    S::run(const_cast<char *>(at(p.dg, p.dg_stride, r, k)), og);
+                    S::run(const_cast<char *>(at(p.du, p.du_stride, r, k)), ou);
                 }
             }
             if (WEIGHTED && r < r1) {  // r is the same for every thread of the CTA
