@@ -138,14 +138,38 @@ constexpr Policy kBwdPolicy = {32, 0, 0, 6};
 constexpr int kBwdModeMaxPack = 16;
 // The per-token-weighted backward is one CTA per row, persistent over rows.
 constexpr Policy kRowPolicy = {16, 3, 3, 6};
-// The bias tile kernel is launched as one wave of this many CTAs per SM; the
-// workspace size follows from it.  Swept with the cp.async ring
-// (BiasStages) over 1.5 - 6 CTAs per SM on the large-FFN and Llama-like
-// shapes: the bias form did best at 2 (407.6 / 189.0 us against 424.7 /
-// 196.7 us for the ring-less kernel at 3), the weights + bias form at 3
-// (429.0 / 202.7 us against 475.2 / 221.1; 466 / 215 at 2).
-constexpr int kBiasCtasPerSm = 2;
-constexpr int kWeightedBiasCtasPerSm = 3;
+// The bias tile kernel is launched as one wave of per_sm CTAs per SM, each
+// covering tile_cols columns of each half, with its registers held to
+// min_ctas CTAs per SM; the workspace size follows from it.  Packs of 8 and
+// 16 bytes: swept with the cp.async ring (BiasStages) over 1.5 - 6 CTAs per
+// SM on the large-FFN and Llama-like shapes, the bias form did best at 2
+// (407.6 / 189.0 us against 424.7 / 196.7 us for the ring-less kernel at 3),
+// the weights + bias form at 3 (429.0 / 202.7 us against 475.2 / 221.1; 466 /
+// 215 at 2).  Packs of 4 bytes and less (one element each, no ring): with
+// that shape the kernel waits on its loads (2 CTAs per SM: 23 % of the warps
+// active, issue 46 %, fp32 odd-width bias form), and at 4 CTAs per SM its 2048
+// columns spill.  1024-column tiles at 4 CTAs per SM (53-63 registers) did
+// best, in fractions of the copy rate (bias / weights + bias form):
+//   shape (columns, CTAs/SM, register bound)   fp32 3000 x 5503   bf16 8192 x 14335
+//   2048, 2 (bias) / 3, 3                      0.62 / 0.56        0.55 / 0.44
+//   2048, 3, 3                                 0.70 / 0.56        0.67 / 0.44
+//   2048, 4, 4                                 0.38 / 0.37        0.46 / 0.41
+//   1024, 4, 4                                 0.72 / 0.69        0.68 / 0.62
+//   1024, 5, 5                                 0.72 / 0.59        0.68 / 0.44
+//   1024, 6, 6                                 0.59 / 0.51        0.53 / 0.41
+//   512, 5, 5 / 512, 6, 6 / 512, 8, 8          0.69-0.74 / 0.62-0.66   0.60-0.64 / 0.42-0.53
+// (equal-width tiles, for the ragged last tile, added nothing).
+struct BiasShape {
+    int tile_cols, per_sm, min_ctas;
+};
+constexpr BiasShape kBiasWide = {swiglu::kBiasTileCols, 2, 3};
+constexpr BiasShape kWeightedBiasWide = {swiglu::kBiasTileCols, 3, 3};
+constexpr BiasShape kBiasNarrow = {1024, 4, 4};
+constexpr BiasShape kWeightedBiasNarrow = {1024, 4, 4};
+constexpr BiasShape bias_shape(bool weighted, int pack_bytes) {
+    return pack_bytes <= 4 ? (weighted ? kWeightedBiasNarrow : kBiasNarrow)
+                           : (weighted ? kWeightedBiasWide : kBiasWide);
+}
 
 // Resident CTAs per SM to launch with, 0 for a one-pass grid.
 constexpr int ctas_cap(const Policy &p, int pack_bytes) {
@@ -253,18 +277,16 @@ struct BwdArgs {
 };
 
 // Row groups of the bias backward: enough (column tile, row group) CTAs to
-// fill every SM with kBiasCtasPerSm (with weights: kWeightedBiasCtasPerSm) of
-// them, once.
+// fill every SM with the shape's per_sm of them, once.
 struct BiasPlan {
     int64_t tiles, groups, rows_per_group;
-    size_t workspace_bytes;
+    size_t workspace_bytes;  // the column sums: groups x 2n fp32
 };
 
-BiasPlan bias_plan(int64_t rows, int64_t n, int sms, bool weighted) {  // rows, n >= 1
+BiasPlan bias_plan(int64_t rows, int64_t n, int sms, const BiasShape &s) {  // rows, n >= 1
     BiasPlan b;
-    b.tiles = (n + swiglu::kBiasTileCols - 1) / swiglu::kBiasTileCols;
-    const int per_sm = weighted ? kWeightedBiasCtasPerSm : kBiasCtasPerSm;
-    int64_t groups = ((int64_t)sms * per_sm) / b.tiles;
+    b.tiles = (n + s.tile_cols - 1) / s.tile_cols;
+    int64_t groups = ((int64_t)sms * s.per_sm) / b.tiles;
     if (groups < 1) groups = 1;
     if (groups > rows) groups = rows;
     b.rows_per_group = (rows + groups - 1) / groups;
@@ -273,14 +295,22 @@ BiasPlan bias_plan(int64_t rows, int64_t n, int sms, bool weighted) {  // rows, 
     return b;
 }
 
-// The weighted bias backward adds, after the column sums (from a 16-byte
-// boundary), one fp32 dw partial per (row, column tile).  False when the size
-// does not fit size_t.
-bool weighted_bias_workspace(int64_t rows, int64_t n, int sms, size_t &dw_offset, size_t &bytes) {
-    const BiasPlan b = bias_plan(rows, n, sms, true);
-    dw_offset = (b.workspace_bytes + 15) / 16 * 16;
+// Workspace of the bias backward: the column sums from the start and, with
+// weights, one fp32 dw partial per (row, column tile) from dw_offset (a 16-byte
+// boundary).  The pack width, which picks the shape, depends on the pointers,
+// so the size covers both shapes of the form.  False when the size does not
+// fit size_t.
+bool bias_workspace(int64_t rows, int64_t n, int sms, bool weighted, size_t &dw_offset,
+                    size_t &bytes) {
+    const BiasPlan w = bias_plan(rows, n, sms, weighted ? kWeightedBiasWide : kBiasWide);
+    const BiasPlan v = bias_plan(rows, n, sms, weighted ? kWeightedBiasNarrow : kBiasNarrow);
+    bytes = w.workspace_bytes > v.workspace_bytes ? w.workspace_bytes : v.workspace_bytes;
+    dw_offset = 0;
+    if (!weighted) return true;
+    dw_offset = (bytes + 15) / 16 * 16;
+    const int64_t tiles = w.tiles > v.tiles ? w.tiles : v.tiles;
     size_t cells, dw_bytes;
-    if (__builtin_mul_overflow((size_t)rows, (size_t)b.tiles, &cells)) return false;
+    if (__builtin_mul_overflow((size_t)rows, (size_t)tiles, &cells)) return false;
     if (__builtin_mul_overflow(cells, sizeof(float), &dw_bytes)) return false;
     return !__builtin_add_overflow(dw_offset, dw_bytes, &bytes);
 }
@@ -497,10 +527,11 @@ constexpr int kDwBatch = 16;
 template <typename E, int VEC, bool IN_PLACE, bool WEIGHTED>
 swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     constexpr int STAGES = E::kBytes * VEC == 16 ? BiasStages<E, WEIGHTED>::value : 0;
-    constexpr int ring = swiglu::swiglu_bias_ring_bytes<VEC, E::kBytes, STAGES>();
+    constexpr BiasShape S = bias_shape(WEIGHTED, E::kBytes * VEC);
+    constexpr int ring = swiglu::swiglu_bias_ring_bytes<VEC, E::kBytes, STAGES, S.tile_cols>();
     auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
                                                  IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore,
-                                                 WEIGHTED, STAGES, kDwBatch>;
+                                                 WEIGHTED, STAGES, kDwBatch, S.tile_cols, S.min_ctas>;
     static std::atomic<int> opted_in[kMaxDevices];
     Device d;
     cudaError_t e = current_device(d);
@@ -515,7 +546,7 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
             if (cacheable) opted_in[d.id].store(1, std::memory_order_relaxed);
         }
     }
-    const BiasPlan b = bias_plan(a.rows, a.n, d.sms, WEIGHTED);
+    const BiasPlan b = bias_plan(a.rows, a.n, d.sms, S);
     // The plan is one wave of a fixed number of CTAs per SM, each walking its
     // rows, and the SM's issue bounds them: launched early beside the previous
     // grid's last CTAs, an SM may take one CTA more than the plan and another
@@ -525,8 +556,7 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     int fit = 0;
     e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, fit, (size_t)ring);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int planned = WEIGHTED ? kWeightedBiasCtasPerSm : kBiasCtasPerSm;
-    e = launch_pdl(planned >= fit, kernel, (unsigned)(b.tiles * b.groups), swiglu::kThreads, (size_t)ring, stream,
+    e = launch_pdl(S.per_sm >= fit, kernel, (unsigned)(b.tiles * b.groups), swiglu::kThreads, (size_t)ring, stream,
                    bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     if (e != cudaSuccess) return cuda_fail(e);
     // the reductions: kReduceCols columns of dbias per CTA, then (with
@@ -736,9 +766,8 @@ swiglu_status_t bias_bwd_impl(const void *dy, const void *x, const void *bias, c
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    size_t need = bias_plan(rows, n, d.sms, weighted).workspace_bytes, dw_offset = 0;
-    if (weighted && !weighted_bias_workspace(rows, n, d.sms, dw_offset, need))
-        return SWIGLU_ERR_SHAPE;
+    size_t need = 0, dw_offset = 0;
+    if (!bias_workspace(rows, n, d.sms, weighted, dw_offset, need)) return SWIGLU_ERR_SHAPE;
     if (workspace_bytes < need) return SWIGLU_ERR_WORKSPACE;
     a.mode = weighted ? swiglu::kBiasWeight : swiglu::kBias;
     a.bias_g = bias;
@@ -874,7 +903,8 @@ swiglu_status_t swiglu_gateup_bias_bwd_workspace_size(int64_t rows, int64_t n, s
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    *bytes = bias_plan(rows, n, d.sms, false).workspace_bytes;
+    size_t off;
+    if (!bias_workspace(rows, n, d.sms, false, off, *bytes)) return SWIGLU_ERR_SHAPE;
     return SWIGLU_OK;
 }
 
@@ -923,7 +953,7 @@ swiglu_status_t swiglu_gateup_weighted_bias_bwd_workspace_size(int64_t rows, int
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
     size_t off;
-    if (!weighted_bias_workspace(rows, n, d.sms, off, *bytes)) return SWIGLU_ERR_SHAPE;
+    if (!bias_workspace(rows, n, d.sms, true, off, *bytes)) return SWIGLU_ERR_SHAPE;
     return SWIGLU_OK;
 }
 
@@ -1106,7 +1136,8 @@ extern "C" swiglu_status_t swiglu_gateup_bias_bwd_noalloc(
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (bias_plan(rows, n, d.sms, false).workspace_bytes > SWIGLU_NOALLOC_SCRATCH_BYTES)
+    size_t off, need;
+    if (!bias_workspace(rows, n, d.sms, false, off, need) || need > SWIGLU_NOALLOC_SCRATCH_BYTES)
         return SWIGLU_ERR_WORKSPACE;
     void *scratch = nullptr;
     e = noalloc_scratch(d.id, &scratch);

@@ -851,9 +851,10 @@ __global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const Bwd
     }
 }
 
-// Bias backward, first pass: CTA (tile, group) covers kBiasTileCols columns of
-// each half for the rows of its row group (see below), writes dx and leaves
-// the column sums of its rows, in fp32, in partial[group][0, 2n).
+// Bias backward, first pass: CTA (tile, group) covers TILE_COLS columns of
+// each half (kBiasTileCols unless the launch picks a narrower tile) for the
+// rows of its row group (see below), writes dx and leaves the column sums of
+// its rows, in fp32, in partial[group][0, 2n).
 constexpr int kBiasTileCols = 2048;
 
 // One pack of the bias backward: dgate / dup into gv / uv, added to the
@@ -892,15 +893,16 @@ __device__ __forceinline__ void bias_pack(const uint32_t *d, const uint32_t *g, 
 // STAGES x 3 operands x PPT packs x kThreads threads x one pack of dynamic
 // shared memory (swiglu_bias_ring_bytes); consecutive threads own consecutive
 // slots, so the reads back are free of bank conflicts.
-template <int VEC, int E_BYTES, int STAGES>
+template <int VEC, int E_BYTES, int STAGES, int TILE_COLS = kBiasTileCols>
 constexpr int swiglu_bias_ring_bytes() {
-    return STAGES * 3 * (kBiasTileCols / (kThreads * VEC)) * kThreads * E_BYTES * VEC;
+    return STAGES * 3 * (TILE_COLS / (kThreads * VEC)) * kThreads * E_BYTES * VEC;
 }
 
+// MINB: the CTAs per SM the register allocation is held to (launch bounds).
 template <typename E, int VEC, bool IN_PLACE, int LD, int ST, bool WEIGHTED = false, int STAGES = 0,
-          int DW_BATCH = 32>
-__global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
-                                                                      int64_t rows_per_group) {
+          int DW_BATCH = 32, int TILE_COLS = kBiasTileCols, int MINB = 3>
+__global__ void __launch_bounds__(kThreads, MINB) swiglu_bwd_bias_kernel(const BwdParams p, int32_t tiles,
+                                                                         int64_t rows_per_group) {
     await_previous_grid();
     allow_next_grid();
     constexpr int MODE = WEIGHTED ? kBiasWeight : kBias;
@@ -909,8 +911,8 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
-    constexpr int PPT = kBiasTileCols / (kThreads * VEC);  // packs per thread per row and half
-    static_assert(PPT >= 1 && PPT * kThreads * VEC == kBiasTileCols, "tile / pack mismatch");
+    constexpr int PPT = TILE_COLS / (kThreads * VEC);  // packs per thread per row and half
+    static_assert(PPT >= 1 && PPT * kThreads * VEC == TILE_COLS, "tile / pack mismatch");
     static_assert(STAGES == 0 || ((B == 4 || B == 8 || B == 16) && STAGES >= 2),
                   "the cp.async ring moves 4-, 8- or 16-byte packs");
     // rows whose loads are issued together: keeps about as many bytes in flight
@@ -940,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 3) swiglu_bwd_bias_kernel(const BwdP
     float ag[PPT][VEC], au[PPT][VEC];
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        c[k] = tile * (kBiasTileCols / VEC) + k * kThreads + threadIdx.x;
+        c[k] = tile * (TILE_COLS / VEC) + k * kThreads + threadIdx.x;
 #pragma unroll
         for (int i = 0; i < NW; ++i) bg[k][i] = bu[k][i] = 0u;
         if (c[k] < p.nvec) {

@@ -200,7 +200,8 @@ swiglu_status_t swiglu_gateup_bias_bwd(const void *dy, const void *x, const void
  * a device workspace of at least
  * swiglu_gateup_weighted_bias_bwd_workspace_size(rows, n) bytes, 16-byte
  * aligned: the bias form's column sums plus one fp32 partial of dw per row and
- * 2048-column tile.  Aliasing: y / dx / dbias / dw / workspace may overlap
+ * column tile (tiles of 2048 columns, or 1024 when the operands allow no pack
+ * wider than 4 bytes; the size covers both).  Aliasing: y / dx / dbias / dw / workspace may overlap
  * neither bias nor w; dbias, dw and the workspace overlap nothing.
  * With rows == 0 (n > 0) the backward sets dbias to zero; with n == 0
  * (rows > 0) it sets dw to zero.

@@ -76,17 +76,27 @@ def assert_reduction(gpu, exact, abs_sum, depth, what, *, elem, count):
                              f"{[(k, float(gpu[k]), float(exact[k]), float(tol[k])) for k in i]}")
 
 
+# The tile kernel's launch shapes, (tile columns, CTAs per SM), by pack class:
+# packs of 8 or 16 bytes, then packs of at most 4 bytes.  Which one a call takes
+# depends on its pointers, so the bounds below take the deeper of the two.
+BIAS_SHAPES = [(2048, 2), (1024, 4)]
+WEIGHTED_BIAS_SHAPES = [(2048, 3), (1024, 4)]
+
+
 def _bias_depth(rows, n, weighted=False):
     """Chained additions behind one dbias value: the rows of one row group
     (the tile kernel), then one of 8 contiguous segments of the row groups,
     then the 8 segment sums (the reduce kernel).  The plan fills every SM once
-    with 2 (bias) or 3 (weights + bias) tile CTAs."""
+    with the shape's CTAs per SM."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    tiles = -(-n // 2048)
-    groups = max(1, min(rows, (sms * (3 if weighted else 2)) // tiles))
-    rpg = -(-rows // groups)
-    groups = -(-rows // rpg)
-    return rpg + -(-groups // 8) + 8
+    depth = 0
+    for tile, per_sm in WEIGHTED_BIAS_SHAPES if weighted else BIAS_SHAPES:
+        tiles = -(-n // tile)
+        groups = max(1, min(rows, (sms * per_sm) // tiles))
+        rpg = -(-rows // groups)
+        groups = -(-rows // rpg)
+        depth = max(depth, rpg + -(-groups // 8) + 8)
+    return depth
 
 
 CASES = [("tiny_f32", None), ("megatron_4096_bf16", 300), ("odd_5503_f32", 97),
@@ -144,7 +154,9 @@ def test_bias_matches_oracle(sw, name, rows):
 
 
 def _wb_dw_depth(n):
-    return 21 + -(-n // 2048)
+    """Chained additions behind one dw value: a thread's tile / 256 columns,
+    the 8 warps' sums of a lane, 5 shuffle steps, then the column tiles."""
+    return max(tile // 256 + 13 + -(-n // tile) for tile, _ in WEIGHTED_BIAS_SHAPES)
 
 
 def _check_weighted_bias(dy_c, x_c, bias_c, w_c, y, dx, db, dw, what):
