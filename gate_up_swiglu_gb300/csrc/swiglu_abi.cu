@@ -228,6 +228,70 @@ cudaError_t ctas_per_sm(K kernel, int threads, const Device &d, std::atomic<int>
     return cudaSuccess;
 }
 
+// Dynamic shared memory of a one-wave launch planned at per_sm CTAs per SM.
+// The kernel uses `need` bytes.  When more than per_sm CTAs would fit, the
+// launch asks for enough unused shared memory that no SM can hold more than
+// per_sm of them.  Launched early beside the previous grid's last CTAs, such a
+// plan is then still spread evenly (left free, an SM may take one CTA more than
+// the plan and another one less: the bias form ran 7 % slower on the large FFN
+// that way, so those launches used to wait for the previous grid instead).
+// Raises the kernel's dynamic shared memory limit as needed.  `fit` is the
+// CTAs per SM that `bytes` allows; both are cached per device.
+struct HeldSmem {
+    int bytes, fit;
+};
+
+template <typename K>
+cudaError_t held_smem(K kernel, int threads, const Device &d, int per_sm, int need,
+                      std::atomic<long long> *cache, HeldSmem &out) {
+    const bool cacheable = d.id >= 0 && d.id < kMaxDevices;
+    const long long v = cacheable ? cache[d.id].load(std::memory_order_relaxed) : 0;
+    if (v != 0) {
+        out.bytes = (int)(v >> 8);
+        out.fit = (int)(v & 0xff);
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaSuccess;
+    if (need > 0 && (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need)) !=
+                        cudaSuccess)
+        return e;
+    int fit = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, kernel, threads, (size_t)need)) != cudaSuccess)
+        return e;
+    out.bytes = need;
+    out.fit = fit < 1 ? 1 : fit;
+    if (fit > per_sm) {
+        cudaFuncAttributes fa;
+        int sm_bytes = 0, reserved = 0, optin = 0;
+        if ((e = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d.id)) !=
+            cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, d.id)) != cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d.id)) != cudaSuccess)
+            return e;
+        // per_sm + 1 CTAs of (pad + static + reserved) bytes overflow the SM
+        long long pad = sm_bytes / (per_sm + 1) + 1 - (long long)fa.sharedSizeBytes - reserved;
+        pad = (pad + 127) / 128 * 128;
+        if (pad > need && pad + (long long)fa.sharedSizeBytes <= optin) {
+            if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pad)) !=
+                cudaSuccess)
+                return e;
+            int held = 0;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&held, kernel, threads, (size_t)pad)) !=
+                cudaSuccess)
+                return e;
+            if (held == per_sm) {  // else keep the unpadded launch
+                out.bytes = (int)pad;
+                out.fit = held;
+            }
+        }
+    }
+    if (cacheable) cache[d.id].store(((long long)out.bytes << 8) | out.fit, std::memory_order_relaxed);
+    return cudaSuccess;
+}
+
 // Persistent grid: never more CTAs than there are units of U * T packs,
 // never more than fill every SM with resident CTAs.
 template <int U, int T = swiglu::kThreads>
@@ -507,7 +571,10 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     int64_t grid = (int64_t)d.sms * per_sm;
     if (grid > a.rows) grid = a.rows;
     // a fixed number of row-walking CTAs per SM, as in the bias tile kernel:
-    // launched early only when that fills every SM (below that, 4.5 % slower)
+    // launched early only when that fills every SM (below that, 4.5 % slower).
+    // Holding the SMs to the plan with padded shared memory (held_smem) and
+    // launching early was slower still here (large FFN 0.980 -> 0.926 of the
+    // copy rate, Llama-like 0.934 -> 0.893), unlike the bias tile kernel.
     e = launch_pdl(per_sm >= fit, kernel, (unsigned)grid, swiglu::kThreads, 0, stream, bwd_params(a, VEC));
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
@@ -532,32 +599,22 @@ swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
     auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
                                                  IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore,
                                                  WEIGHTED, STAGES, kDwBatch, S.tile_cols, S.min_ctas>;
-    static std::atomic<int> opted_in[kMaxDevices];
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (ring > 0) {
-        // dynamic shared memory beyond 48 KiB (with the static batch buffer)
-        // needs the kernel's opt-in, once per device
-        const bool cacheable = d.id >= 0 && d.id < kMaxDevices;
-        if (!cacheable || opted_in[d.id].load(std::memory_order_relaxed) == 0) {
-            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ring);
-            if (e != cudaSuccess) return cuda_fail(e);
-            if (cacheable) opted_in[d.id].store(1, std::memory_order_relaxed);
-        }
-    }
     const BiasPlan b = bias_plan(a.rows, a.n, d.sms, S);
     // The plan is one wave of a fixed number of CTAs per SM, each walking its
-    // rows, and the SM's issue bounds them: launched early beside the previous
-    // grid's last CTAs, an SM may take one CTA more than the plan and another
-    // one less (bias form, large FFN: 7 % slower).  So it launches early only
-    // when the plan fills every SM.
-    static std::atomic<int> occ[kMaxDevices];
-    int fit = 0;
-    e = ctas_per_sm(kernel, swiglu::kThreads, d, occ, fit, (size_t)ring);
+    // rows, and the SM's issue bounds them.  The launch holds every SM to the
+    // plan (held_smem: the bias form's 2 CTAs per SM would otherwise leave room
+    // for 3; with that, 0.848 -> 0.860 of the copy rate on ffn-4096, 0.960 ->
+    // 0.973 Llama-like, 0.991 -> 0.996 large FFN) and launches early when it
+    // does.
+    static std::atomic<long long> held[kMaxDevices];
+    HeldSmem hs;
+    e = held_smem(kernel, swiglu::kThreads, d, S.per_sm, ring, held, hs);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = launch_pdl(S.per_sm >= fit, kernel, (unsigned)(b.tiles * b.groups), swiglu::kThreads, (size_t)ring, stream,
-                   bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
+    e = launch_pdl(S.per_sm >= hs.fit, kernel, (unsigned)(b.tiles * b.groups), swiglu::kThreads,
+                   (size_t)hs.bytes, stream, bwd_params(a, VEC), (int32_t)b.tiles, b.rows_per_group);
     if (e != cudaSuccess) return cuda_fail(e);
     // the reductions: kReduceCols columns of dbias per CTA, then (with
     // weights) kReduceThreads rows of dw per CTA, in one launch

@@ -1104,20 +1104,28 @@ constexpr int kReduceCols = 32;
 constexpr int kReduceSegs = 8;
 constexpr int kReduceThreads = kReduceCols * kReduceSegs;
 
-// Sum of the `count` floats at p, p + stride, ..., added in that order; the
-// loads go out eight at a time so a long chain does not wait on one load
-// latency per term.
+// Sum of the `count` floats at p, p + stride, ..., added in that order.  The
+// loads go out sixteen at a time (the last batch only up to count) from one
+// walking pointer, so a chain waits on one load latency per sixteen terms and
+// holds no address per term: the ffn-4096 bias backward's 19-group segments
+// took two load rounds instead of two plus three single loads (0.827 -> 0.853
+// of the copy rate; the earlier form loaded eight at a time).
 __device__ __forceinline__ float ordered_sum(const float *p, int64_t count, int64_t stride) {
+    constexpr int kBatch = 16;
     float s = 0.0f;
-    int64_t q = 0;
-    for (; q + 8 <= count; q += 8) {
-        float v[8];
+    for (int64_t q = 0; q < count; q += kBatch) {
+        const int live = count - q < kBatch ? (int)(count - q) : kBatch;
+        float v[kBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = p[(q + i) * stride];
+        for (int i = 0; i < kBatch; ++i) {
+            v[i] = 0.0f;
+            if (i < live) v[i] = *p;
+            p += stride;
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s = __fadd_rn(s, v[i]);
+        for (int i = 0; i < kBatch; ++i)
+            if (i < live) s = __fadd_rn(s, v[i]);
     }
-    for (; q < count; ++q) s = __fadd_rn(s, p[q * stride]);
     return s;
 }
 
