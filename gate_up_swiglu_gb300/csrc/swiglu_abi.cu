@@ -552,13 +552,13 @@ swiglu_status_t launch_bwd_plain(const BwdArgs &a, cudaStream_t stream) {
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
 }
 
-template <typename E, int VEC, bool IN_PLACE>
-swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
+template <typename E, int VEC, bool IN_PLACE, int ROWS, int MINB>
+swiglu_status_t launch_bwd_weighted_rows(const BwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     static std::atomic<int> occ[kMaxDevices];
     auto kernel = swiglu::swiglu_bwd_weighted_kernel<E, VEC, U, IN_PLACE,
                                                      IN_PLACE ? kLoadInPlace : kLoadOutOfPlace,
-                                                     kStore>;
+                                                     kStore, ROWS, MINB>;
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -577,6 +577,28 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
     // copy rate, Llama-like 0.934 -> 0.893), unlike the bias tile kernel.
     e = launch_pdl(per_sm >= fit, kernel, (unsigned)grid, swiglu::kThreads, 0, stream, bwd_params(a, VEC));
     return e == cudaSuccess ? SWIGLU_OK : cuda_fail(e);
+}
+
+// Rows per pass of the per-token-weighted row kernel and the CTAs per SM its
+// registers are held to.  16-byte packs take two rows per pass; fractions of
+// the copy rate, one row / two rows at 127 registers (2 CTAs per SM) / two
+// rows held to 3 CTAs per SM (80 registers):
+//   ffn-4096 [8192, 2 x 4096] bf16       0.831 / 0.880 / 0.915
+//   Llama-like [8192, 2 x 14336] bf16    0.931 / 0.950 / 0.965
+//   large FFN [8192, 2 x 32768] bf16     0.979 / 0.988 / 0.948
+//   odd width [6000, 2 x 5000] bf16      0.723 / 0.763 / 0.823
+// so rows of at most kWeightedShortRowPacks packs take the held form and
+// longer rows the unbounded one.  Narrow packs keep one row per pass (fp32
+// odd width: 0.818 / 0.725 / 0.718).
+constexpr int64_t kWeightedShortRowPacks = 2048;
+
+template <typename E, int VEC, bool IN_PLACE>
+swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
+    if constexpr (E::kBytes * VEC == 16) {
+        if (a.n / VEC <= kWeightedShortRowPacks) return launch_bwd_weighted_rows<E, VEC, IN_PLACE, 2, 3>(a, stream);
+        return launch_bwd_weighted_rows<E, VEC, IN_PLACE, 2, 0>(a, stream);
+    }
+    return launch_bwd_weighted_rows<E, VEC, IN_PLACE, 1, 0>(a, stream);
 }
 
 // Rows in flight through the bias tile kernel's cp.async ring (0: plain

@@ -800,54 +800,108 @@ __device__ __forceinline__ void weighted_pack(const uint32_t *d, const uint32_t 
     }
 }
 
-template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST>
-__global__ void __launch_bounds__(kThreads) swiglu_bwd_weighted_kernel(const BwdParams p) {
+// Two sums over the CTA, each added in block_sum's fixed order (the same bits
+// as two block_sum calls), behind one pair of barriers.
+__device__ __forceinline__ float2 block_sum2(float a, float b, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = __fadd_rn(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red may still be read from the previous call
+    if (lane == 0) {
+        red[warp] = a;
+        red[kThreads / 32 + warp] = b;
+    }
+    __syncthreads();
+    float ta = 0.0f, tb = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kThreads / 32; ++k) {
+        ta = __fadd_rn(ta, red[k]);
+        tb = __fadd_rn(tb, red[kThreads / 32 + k]);
+    }
+    return make_float2(ta, tb);
+}
+
+// ROWS rows per pass (1 or 2): with 2, a CTA takes rows r and r + gridDim.x
+// together, issues both rows' loads before computing either, and finishes
+// both dw values behind one pair of barriers, so twice the bytes are in flight
+// per CTA and a row's barriers are shared.  Each row's sum keeps its order.
+// MINB: CTAs per SM the registers are held to (0: no bound).
+template <typename E, int VEC, int U, bool IN_PLACE, int LD, int ST, int ROWS = 1, int MINB = 0>
+__global__ void __launch_bounds__(kThreads, MINB) swiglu_bwd_weighted_kernel(const BwdParams p) {
     await_previous_grid();
     allow_next_grid();
     static_assert(!IN_PLACE || (LD != kLdNC && LD != kLdNC256), "in place: coherent loads only");
+    static_assert(ROWS == 1 || ROWS == 2, "one or two rows per pass");
     constexpr int B = E::kBytes * VEC;
     constexpr int NW = (B + 3) / 4;
     using L = Ld<B, LD>;
     using S = St<B, ST>;
-    __shared__ float red[kThreads / 32];
-    for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
-        const char *dyr = static_cast<const char *>(p.dy) + r * p.dy_stride * B;
-        const char *gr = static_cast<const char *>(p.g) + r * p.g_stride * B;
-        const char *ur = static_cast<const char *>(p.u) + r * p.u_stride * B;
-        char *dgr = static_cast<char *>(p.dg) + r * p.dg_stride * B;
-        char *dur = static_cast<char *>(p.du) + r * p.du_stride * B;
-        const float wr = __ldg(p.w + r);
-        float acc = 0.0f;
-        for (int32_t c0 = threadIdx.x; c0 < p.nvec; c0 += U * kThreads) {
-            uint32_t d[U][NW], g[U][NW], u[U][NW];
+    __shared__ float red[ROWS * kThreads / 32];
+    for (int64_t r0 = blockIdx.x; r0 < p.rows; r0 += ROWS * (int64_t)gridDim.x) {
+        // row h of the pass is r0 + h * gridDim.x; live[h]: it exists
+        bool live[ROWS];
+        const char *dyr[ROWS], *gr[ROWS], *ur[ROWS];
+        char *dgr[ROWS], *dur[ROWS];
+        float wr[ROWS], acc[ROWS];
 #pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int32_t c = c0 + k * kThreads;
-                if (c < p.nvec) {
-                    L::run(dyr + (int64_t)c * B, d[k]);
-                    L::run(gr + (int64_t)c * B, g[k]);
-                    L::run(ur + (int64_t)c * B, u[k]);
+        for (int h = 0; h < ROWS; ++h) {
+            live[h] = r0 + h * (int64_t)gridDim.x < p.rows;
+            const int64_t r = live[h] ? r0 + h * (int64_t)gridDim.x : r0;
+            dyr[h] = static_cast<const char *>(p.dy) + r * p.dy_stride * B;
+            gr[h] = static_cast<const char *>(p.g) + r * p.g_stride * B;
+            ur[h] = static_cast<const char *>(p.u) + r * p.u_stride * B;
+            dgr[h] = static_cast<char *>(p.dg) + r * p.dg_stride * B;
+            dur[h] = static_cast<char *>(p.du) + r * p.du_stride * B;
+            wr[h] = __ldg(p.w + r);
+            acc[h] = 0.0f;
+        }
+        for (int32_t c0 = threadIdx.x; c0 < p.nvec; c0 += U * kThreads) {
+            uint32_t d[ROWS][U][NW], g[ROWS][U][NW], u[ROWS][U][NW];
+#pragma unroll
+            for (int h = 0; h < ROWS; ++h) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const int32_t c = c0 + k * kThreads;
+                    if (live[h] && c < p.nvec) {
+                        L::run(dyr[h] + (int64_t)c * B, d[h][k]);
+                        L::run(gr[h] + (int64_t)c * B, g[h][k]);
+                        L::run(ur[h] + (int64_t)c * B, u[h][k]);
+                    }
                 }
             }
 #pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const int32_t c = c0 + k * kThreads;
-                if (c < p.nvec) {
-                    uint32_t og[NW] = {}, ou[NW] = {};
-                    float gv[VEC], uv[VEC];
-                    if (pack_has_deep<E, VEC>(g[k]))
-                        weighted_pack<E, VEC, true>(d[k], g[k], u[k], wr, acc, gv, uv);
-                    else
-                        weighted_pack<E, VEC, false>(d[k], g[k], u[k], wr, acc, gv, uv);
-                    store_pack<E, VEC>(og, gv);
-                    store_pack<E, VEC>(ou, uv);
-                    S::run(dgr + (int64_t)c * B, og);
-                    S::run(dur + (int64_t)c * B, ou);
+            for (int h = 0; h < ROWS; ++h) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const int32_t c = c0 + k * kThreads;
+                    if (live[h] && c < p.nvec) {
+                        uint32_t og[NW] = {}, ou[NW] = {};
+                        float gv[VEC], uv[VEC];
+                        if (pack_has_deep<E, VEC>(g[h][k]))
+                            weighted_pack<E, VEC, true>(d[h][k], g[h][k], u[h][k], wr[h], acc[h], gv, uv);
+                        else
+                            weighted_pack<E, VEC, false>(d[h][k], g[h][k], u[h][k], wr[h], acc[h], gv, uv);
+                        store_pack<E, VEC>(og, gv);
+                        store_pack<E, VEC>(ou, uv);
+                        S::run(dgr[h] + (int64_t)c * B, og);
+                        S::run(dur[h] + (int64_t)c * B, ou);
+                    }
                 }
             }
         }
-        acc = block_sum(acc, red);
-        if (threadIdx.x == 0) p.dw[r] = acc;
+        if constexpr (ROWS == 2) {
+            const float2 t = block_sum2(acc[0], acc[1], red);
+            if (threadIdx.x == 0) {
+                p.dw[r0] = t.x;
+                if (live[1]) p.dw[r0 + gridDim.x] = t.y;
+            }
+        } else {
+            const float t = block_sum(acc[0], red);
+            if (threadIdx.x == 0) p.dw[r0] = t;
+        }
     }
 }
 
