@@ -141,7 +141,7 @@ constexpr Policy kRowPolicy = {16, 3, 3, 6};
 // The bias tile kernel is launched as one wave of per_sm CTAs per SM, each
 // covering tile_cols columns of each half, with its registers held to
 // min_ctas CTAs per SM; the workspace size follows from it.  Packs of 8 and
-// 16 bytes: swept with the cp.async ring (BiasStages) over 1.5 - 6 CTAs per
+// 16 bytes: swept with the cp.async ring (bias_stages) over 1.5 - 6 CTAs per
 // SM on the large-FFN and Llama-like shapes, the bias form did best at 2
 // (407.6 / 189.0 us against 424.7 / 196.7 us for the ring-less kernel at 3),
 // the weights + bias form at 3 (429.0 / 202.7 us against 475.2 / 221.1; 466 /
@@ -166,9 +166,19 @@ constexpr BiasShape kBiasWide = {swiglu::kBiasTileCols, 2, 3};
 constexpr BiasShape kWeightedBiasWide = {swiglu::kBiasTileCols, 3, 3};
 constexpr BiasShape kBiasNarrow = {1024, 4, 4};
 constexpr BiasShape kWeightedBiasNarrow = {1024, 4, 4};
+// 8-byte packs: bf16 [8192, 2 x 14340] / fp32 [8192, 2 x 4098], bias / weights
+// + bias form, fractions of the copy rate:
+//   2048-column shape, no ring      0.662 / 0.691    0.619 / 0.639
+//   2048-column shape, 2-row ring   0.880 / 0.783    0.734 / 0.518
+//   1024 x 4, no ring               0.815 / 0.714    0.768 / 0.722
+//   1024 x 4, 2-row ring            0.872 / 0.727    0.794 / 0.707
+// so bf16 takes the ring on the 2048-column shape, fp32 the 1024-column shape
+// (with the ring for the bias form only).
+template <typename E>
 constexpr BiasShape bias_shape(bool weighted, int pack_bytes) {
-    return pack_bytes <= 4 ? (weighted ? kWeightedBiasNarrow : kBiasNarrow)
-                           : (weighted ? kWeightedBiasWide : kBiasWide);
+    return pack_bytes <= 4 || (pack_bytes == 8 && E::kBytes == 4)
+               ? (weighted ? kWeightedBiasNarrow : kBiasNarrow)
+               : (weighted ? kWeightedBiasWide : kBiasWide);
 }
 
 // Resident CTAs per SM to launch with, 0 for a one-pass grid.
@@ -602,21 +612,22 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
 }
 
 // Rows in flight through the bias tile kernel's cp.async ring (0: plain
-// register loads), for 16-byte packs; see swiglu_bwd_bias_kernel.  (With
-// 4-byte packs -- fp32, odd n -- a 2-row ring ran 139 us against 97 us
-// without on the odd-width workload's bias backward.)
+// register loads); see swiglu_bwd_bias_kernel.  16-byte packs: 2.  8-byte
+// packs: 2 but for fp32 with weights (see bias_shape).  4-byte packs and
+// narrower: none (fp32, odd n: a 2-row ring ran 139 us against 97 us without
+// on the odd-width workload's bias backward).
 template <typename E, bool WEIGHTED>
-struct BiasStages {
-    static constexpr int value = 2;
-};
+constexpr int bias_stages(int pack_bytes) {
+    return pack_bytes == 16 ? 2 : (pack_bytes == 8 && !(E::kBytes == 4 && WEIGHTED) ? 2 : 0);
+}
 // Rows of dw partial sums the weights + bias tile kernel batches per barrier
 // (16 leaves room for the ring at 3 CTAs per SM; same speed as 32).
 constexpr int kDwBatch = 16;
 
 template <typename E, int VEC, bool IN_PLACE, bool WEIGHTED>
 swiglu_status_t launch_bwd_bias(const BwdArgs &a, cudaStream_t stream) {
-    constexpr int STAGES = E::kBytes * VEC == 16 ? BiasStages<E, WEIGHTED>::value : 0;
-    constexpr BiasShape S = bias_shape(WEIGHTED, E::kBytes * VEC);
+    constexpr int STAGES = bias_stages<E, WEIGHTED>(E::kBytes * VEC);
+    constexpr BiasShape S = bias_shape<E>(WEIGHTED, E::kBytes * VEC);
     constexpr int ring = swiglu::swiglu_bias_ring_bytes<VEC, E::kBytes, STAGES, S.tile_cols>();
     auto kernel = swiglu::swiglu_bwd_bias_kernel<E, VEC, IN_PLACE,
                                                  IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, kStore,
