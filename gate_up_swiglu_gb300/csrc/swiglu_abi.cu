@@ -443,7 +443,7 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
 // kernels replace took 44.5 / 62.4 us on the fp32 workload.
 // The forward of the bias forms keeps K = 8 for bf16 too (the bias values of
 // 16 columns took the kernel to 101 registers and half the speed).
-template <typename E, int MODE, int FMODE = swiglu::kPlain>
+template <typename E, int MODE, int FMODE = swiglu::kPlain, int PV = 1>
 struct SegShape {
     static constexpr int K = 8, T = 128, per_sm = 0;
 };
@@ -458,19 +458,21 @@ struct SegShape<swiglu::BF16, swiglu::kSegFwd, swiglu::kWeight> {
 
 // Operands: fwd in = {g, u}, out = {y}; bwd in = {dy, g, u}, out = {dg, du}.
 // FMODE: the forward's variant; bias_g / bias_u / w as in FwdArgs.
-template <typename E, int MODE, bool IN_PLACE, int FMODE = swiglu::kPlain>
+// PV: elements per pack, 2 for bf16 whose operands all allow 4-byte packs.
+template <typename E, int MODE, bool IN_PLACE, int FMODE = swiglu::kPlain, int PV = 1>
 swiglu_status_t launch_rowseg(const Operand *in, const Operand *out, int64_t rows, int64_t n,
                               cudaStream_t stream, const void *bias_g = nullptr,
                               const void *bias_u = nullptr, const float *w = nullptr) {
-    using Sh = SegShape<E, MODE, FMODE>;
+    using Sh = SegShape<E, MODE, FMODE, PV>;
     constexpr int NIN = MODE == swiglu::kSegFwd ? 2 : 3;
     constexpr int NOUT = MODE == swiglu::kSegFwd ? 1 : 2;
     auto kernel = swiglu::swiglu_rowseg_kernel<E, MODE, Sh::K, Sh::T,
-                                               IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, FMODE>;
+                                               IN_PLACE ? kLoadInPlace : kLoadOutOfPlace, FMODE, PV>;
     static std::atomic<int> occ[kMaxDevices];
     Device d;
     cudaError_t e = current_device(d);
     if (e != cudaSuccess) return cuda_fail(e);
+    n /= PV;  // packs per row from here on
     const int64_t chunks = (n + Sh::K * Sh::T - 1) / (Sh::K * Sh::T);
     const int64_t segments = rows * chunks;
     int64_t grid = segments;
@@ -681,6 +683,25 @@ swiglu_status_t launch_fwd_mode(const FwdArgs &a, cudaStream_t st) {
     return launch_fwd<E, VEC, swiglu::kPlain>(a, st);
 }
 
+// The forward of every form on the row-segment kernels, PV elements per pack.
+template <typename E, int PV>
+swiglu_status_t rowseg_fwd(const FwdArgs &a, cudaStream_t st) {
+    const Operand in[2] = {a.g, a.u};
+    switch (a.mode) {
+        case swiglu::kBias:
+            return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBias, PV>(in, &a.y, a.rows, a.n, st,
+                                                                               a.bias_g, a.bias_u);
+        case swiglu::kWeight:
+            return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kWeight, PV>(in, &a.y, a.rows, a.n, st,
+                                                                                 nullptr, nullptr, a.w);
+        case swiglu::kBiasWeight:
+            return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBiasWeight, PV>(
+                in, &a.y, a.rows, a.n, st, a.bias_g, a.bias_u, a.w);
+        default:
+            return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kPlain, PV>(in, &a.y, a.rows, a.n, st);
+    }
+}
+
 // The widest pack every operand (bias halves included) allows; pick_vec never
 // returns more than max_pack_bytes / kBytes elements, so only those widths are
 // instantiated.
@@ -695,20 +716,9 @@ swiglu_status_t dispatch_fwd(const FwdArgs &a, cudaStream_t st) {
     const int vec = pick_vec(E::kBytes, small ? 16 : kFwdPolicy.max_pack_bytes, a.n, strides, 3,
                              ptrs, np);
     if (vec * E::kBytes <= kSegMaxPackBytes) {
-        const Operand in[2] = {a.g, a.u};
-        switch (a.mode) {
-            case swiglu::kBias:
-                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBias>(in, &a.y, a.rows, a.n, st,
-                                                                               a.bias_g, a.bias_u);
-            case swiglu::kWeight:
-                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kWeight>(
-                    in, &a.y, a.rows, a.n, st, nullptr, nullptr, a.w);
-            case swiglu::kBiasWeight:
-                return launch_rowseg<E, swiglu::kSegFwd, false, swiglu::kBiasWeight>(
-                    in, &a.y, a.rows, a.n, st, a.bias_g, a.bias_u, a.w);
-            default:
-                return launch_rowseg<E, swiglu::kSegFwd, false>(in, &a.y, a.rows, a.n, st);
-        }
+        if constexpr (E::kBytes == 2)
+            if (vec == 2) return rowseg_fwd<E, 2>(a, st);
+        return rowseg_fwd<E, 1>(a, st);
     }
     constexpr int kMaxVec = kFwdPolicy.max_pack_bytes / E::kBytes;
     if constexpr (kMaxVec >= 16) if (vec == 16) return launch_fwd_mode<E, 16>(a, st);
@@ -728,6 +738,8 @@ swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     if (a.mode == swiglu::kPlain && vec * E::kBytes <= kSegMaxPackBytes) {
         const Operand in[3] = {a.dy, a.g, a.u};
         const Operand out[2] = {a.dg, a.du};
+        if constexpr (E::kBytes == 2)
+            if (vec == 2) return launch_rowseg<E, swiglu::kSegBwd, IP, swiglu::kPlain, 2>(in, out, a.rows, a.n, st);
         return launch_rowseg<E, swiglu::kSegBwd, IP>(in, out, a.rows, a.n, st);
     }
     constexpr int kMaxVec = kBwdPolicy.max_pack_bytes / E::kBytes;

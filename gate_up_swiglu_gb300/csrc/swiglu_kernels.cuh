@@ -666,12 +666,14 @@ struct SegParams {
 };
 
 // FMODE: the forward's variant (kPlain, kBias, kWeight, kBiasWeight); the
-// backward is the plain form only.
-template <typename E, int MODE, int K, int T, int LD, int FMODE = kPlain>
+// backward is the plain form only.  PV: elements per pack (2 for bf16 whose
+// operands all allow 4-byte packs; p.n then counts packs).
+template <typename E, int MODE, int K, int T, int LD, int FMODE = kPlain, int PV = 1>
 __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
     await_previous_grid();
     allow_next_grid();
-    constexpr int EB = E::kBytes;
+    static_assert(PV == 1 || (PV == 2 && E::kBytes == 2), "packs of one element, or two bf16");
+    constexpr int EB = E::kBytes * PV;
     constexpr int NIN = MODE == kSegFwd ? 2 : 3;
     constexpr int NOUT = MODE == kSegFwd ? 1 : 2;
     static_assert(MODE == kSegFwd || FMODE == kPlain, "the backward row segments are the plain form");
@@ -705,25 +707,25 @@ __global__ void __launch_bounds__(T) swiglu_rowseg_kernel(const SegParams p) {
         for (int i = 0; i < K; ++i) {
             if (i < live) {
                 if (MODE == kSegFwd) {
-                    float yv[1];
-                    const bool deep = (FMODE & kBias) ? pack_has_deep_biased<E, 1>(&w[0][i], &bgw[i])
-                                                      : pack_has_deep<E, 1>(&w[0][i]);
+                    float yv[PV];
+                    const bool deep = (FMODE & kBias) ? pack_has_deep_biased<E, PV>(&w[0][i], &bgw[i])
+                                                      : pack_has_deep<E, PV>(&w[0][i]);
                     if (deep)
-                        fwd_pack<E, 1, FMODE, true>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
+                        fwd_pack<E, PV, FMODE, true>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
                     else
-                        fwd_pack<E, 1, FMODE, false>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
+                        fwd_pack<E, PV, FMODE, false>(&w[0][i], &w[1][i], &bgw[i], &buw[i], wr, yv);
                     uint32_t o[1] = {0u};
-                    store_pack<E, 1>(o, yv);
+                    store_pack<E, PV>(o, yv);
                     St<EB, kStStream>::run(op[0] + i * T * EB, o);
                 } else {
-                    float gv[1], uv[1];
-                    if (pack_has_deep<E, 1>(&w[1][i]))
-                        bwd_pack<E, 1, true>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
+                    float gv[PV], uv[PV];
+                    if (pack_has_deep<E, PV>(&w[1][i]))
+                        bwd_pack<E, PV, true>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
                     else
-                        bwd_pack<E, 1, false>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
+                        bwd_pack<E, PV, false>(&w[0][i], &w[1][i], &w[2][i], gv, uv);
                     uint32_t og[1] = {0u}, ou[1] = {0u};
-                    store_pack<E, 1>(og, gv);
-                    store_pack<E, 1>(ou, uv);
+                    store_pack<E, PV>(og, gv);
+                    store_pack<E, PV>(ou, uv);
                     St<EB, kStStream>::run(op[0] + i * T * EB, og);
                     St<EB, kStStream>::run(op[1] + i * T * EB, ou);
                 }
