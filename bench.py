@@ -405,7 +405,8 @@ def ours_arm(args, w):
         dbias = torch.empty_like(bias)
         dwv = torch.empty_like(wts)
         size = (sw.bias_bwd_workspace_bytes if form == "bias"
-                else sw.weighted_bias_bwd_workspace_bytes)(rows, n)
+                else sw.weighted_bias_bwd_workspace_bytes if form == "weighted_bias"
+                else (lambda r, c: 0))(rows, n)
         wsp = torch.empty(max(16, size), dtype=torch.uint8, device=dev)
 
     def fwd():
@@ -414,6 +415,9 @@ def ours_arm(args, w):
         elif form == "bias":
             st = lib.swiglu_gateup_bias_fwd(x.data_ptr(), bias.data_ptr(), y.data_ptr(), rows, n,
                                             2 * n, n, dt_code, sh)
+        elif form == "weighted":
+            st = lib.swiglu_gateup_weighted_fwd(x.data_ptr(), wts.data_ptr(), y.data_ptr(), rows, n,
+                                                2 * n, n, dt_code, sh)
         else:
             st = lib.swiglu_gateup_weighted_bias_fwd(x.data_ptr(), bias.data_ptr(), wts.data_ptr(),
                                                      y.data_ptr(), rows, n, 2 * n, n, dt_code, sh)
@@ -429,6 +433,10 @@ def ours_arm(args, w):
             st = lib.swiglu_gateup_bias_bwd(dy.data_ptr(), x.data_ptr(), bias.data_ptr(),
                                             out.data_ptr(), dbias.data_ptr(), wsp.data_ptr(),
                                             wsp.numel(), rows, n, n, 2 * n, 2 * n, dt_code, ip, sh)
+        elif form == "weighted":
+            st = lib.swiglu_gateup_weighted_bwd(dy.data_ptr(), x.data_ptr(), wts.data_ptr(),
+                                                out.data_ptr(), dwv.data_ptr(), rows, n, n, 2 * n,
+                                                2 * n, dt_code, ip, sh)
         else:
             st = lib.swiglu_gateup_weighted_bias_bwd(
                 dy.data_ptr(), x.data_ptr(), bias.data_ptr(), wts.data_ptr(), out.data_ptr(),
@@ -457,7 +465,9 @@ def ours_arm(args, w):
     torch.cuda.synchronize(dev)
     barrier()
     t_wall1 = time.time()
-    launches = 2 * K
+    # one forward launch per step; the bias forms' backward is the tile
+    # kernel plus the reduction launch
+    launches = K * (2 + (1 if form in ("bias", "weighted_bias") else 0))
     # the timed steps may be shorter than the clock sampler's period: keep the
     # same work running, untimed, until the sampled window spans CLOCK_WINDOW_S
     extra = 0
@@ -542,6 +552,7 @@ def ours_arm(args, w):
         "ncu_frac_of_8000_gbs": ncu_fractions(w) if args.form == "plain" else None,
         "roofline": {"bound": "hbm",
                      "kernel": "swiglu_bwd_kernel (out of place)" if args.form == "plain"
+                     else "weighted backward (row kernel, dw included)" if args.form == "weighted"
                      else f"{args.form} backward (tile kernel + reductions)",
                      "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(bwd_gbs / peak, 4), "peak_source": peak_src,
@@ -942,9 +953,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the step alone (the command the kernel profiles are taken on)")
-    ap.add_argument("--form", choices=["plain", "bias", "weighted_bias"], default="plain",
+    ap.add_argument("--form", choices=["plain", "bias", "weighted", "weighted_bias"], default="plain",
                     help="the entry points of the timed step: plain (the headline), or the bias / "
-                         "per-token weights + bias forms")
+                         "per-token weights / per-token weights + bias forms")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.json from an ncu CSV log of this bench and exit")
