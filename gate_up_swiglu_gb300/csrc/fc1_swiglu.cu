@@ -197,26 +197,12 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16 *p, const uint32_t
     }
 }
 
-// Two fp32 lanes per instruction (PTX .f32x2 arithmetic, sm_100 and later):
-// each lane rounds to nearest even exactly as the scalar operation does.
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
+// Two fp32 lanes per instruction: swiglu::x2 and friends (.f32x2 arithmetic,
+// each lane rounded as the scalar operation rounds).
+using swiglu::add_x2;
+using swiglu::mul_x2;
+using swiglu::x2;
+using swiglu::x2_split;
 
 // y for 32 accumulator columns of one row: silu(g) * u from the fp32 gate and
 // up dot products, rounded once to bf16, in pairs.  kMayDeep = false when no
@@ -230,16 +216,16 @@ template <bool kMayDeep>
 __device__ __forceinline__ void activate_chunk(const uint32_t (&gv)[32], const uint32_t (&uv)[32],
                                                uint32_t (&out)[16]) {
     if constexpr (!kMayDeep) {
-        const uint64_t neg_log2e = f32x2(-swiglu::kLog2e, -swiglu::kLog2e), one = f32x2(1.0f, 1.0f);
+        const uint64_t neg_log2e = x2(-swiglu::kLog2e, -swiglu::kLog2e), one = x2(1.0f, 1.0f);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-            const uint64_t g2 = f32x2(__uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
-            const uint64_t u2 = f32x2(__uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
+            const uint64_t g2 = x2(__uint_as_float(gv[i]), __uint_as_float(gv[i + 1]));
+            const uint64_t u2 = x2(__uint_as_float(uv[i]), __uint_as_float(uv[i + 1]));
             float t0, t1, d0, d1, r0, r1;
-            f32x2_split(mul_f32x2(g2, neg_log2e), t0, t1);
-            f32x2_split(add_f32x2(one, f32x2(swiglu::ex2_approx(t0), swiglu::ex2_approx(t1))), d0, d1);
-            const uint64_t s2 = f32x2(swiglu::rcp_approx(d0), swiglu::rcp_approx(d1));
-            f32x2_split(mul_f32x2(mul_f32x2(g2, s2), u2), r0, r1);
+            x2_split(mul_x2(g2, neg_log2e), t0, t1);
+            x2_split(add_x2(one, x2(swiglu::ex2_approx(t0), swiglu::ex2_approx(t1))), d0, d1);
+            const uint64_t s2 = x2(swiglu::rcp_approx(d0), swiglu::rcp_approx(d1));
+            x2_split(mul_x2(mul_x2(g2, s2), u2), r0, r1);
             swiglu::BF16::put2(out, i, r0, r1);
         }
     } else {
