@@ -103,7 +103,7 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 // 105.5, Megatron shape 31.9 against 34.0: CTAs that start in address order
 // keep the DRAM access window compact, where persistent CTAs drift apart.
 // With 16-byte packs (two in flight) 6 CTAs per SM did best.  The forward
-// variants with a bias or row weights: see kFwdModePolicy.  Backward, plain
+// variants with a bias or row weights: see kFwdBiasPolicy.  Backward, plain
 // form: one-pass as well (see kBwdPolicy; at 3 CTAs per SM the large FFN ran
 // 399-418 us against 386 on one pass, before the 32-byte packs).  Narrow
 // packs (4 bytes or less: odd n, misaligned rows) of the plain and two-tensor
@@ -113,16 +113,24 @@ int pick_vec(int eb, int max_bytes, int64_t n, const int64_t *strides, int ns,
 struct Policy {
     int max_pack_bytes;
     int ctas_wide;    // 32-byte packs; 0 = a one-pass grid
-    int ctas_medium;  // 8- and 16-byte packs
+    int ctas_16;      // 16-byte packs
+    int ctas_8;       // 8-byte packs
     int ctas_narrow;  // packs of 4 bytes or less
 };
-constexpr Policy kFwdPolicy = {32, 0, 6, 8};
+// 8-byte packs (bf16 n = 4 mod 8, fp32 n = 2 mod 4): the plain forward runs
+// one pass (bf16 [8192, 2 x 14340] 0.925 -> 0.945 of the copy rate, fp32
+// [8192, 2 x 4098] 0.917 -> 0.967 against 6 CTAs per SM), the weighted forward
+// 6 CTAs per SM (0.822 -> 0.945, 0.805 -> 0.930 against 4); the bias forms
+// were no faster at 6 and slower on one pass, and every form was slower with
+// eight packs in flight instead of four.
+constexpr Policy kFwdPolicy = {32, 0, 6, 0, 8};
 // Bias or row weights alone: one pass as well (large FFN 225.4 / 223.3 us
 // against 258.0 / 254.3 us at 4 CTAs per SM; Llama-like 101.4 / 100.2 against
 // 109.5 / 108.9).  Both together: persistent at 4 CTAs per SM (234.8 us
 // against 249.9 on one pass of 256-thread CTAs and 325.8 of 128-thread ones).
-constexpr Policy kFwdModePolicy = {32, 0, 4, 8};
-constexpr Policy kFwdBiasWeightPolicy = {32, 4, 4, 8};
+constexpr Policy kFwdBiasPolicy = {32, 0, 4, 4, 8};
+constexpr Policy kFwdWeightPolicy = {32, 0, 4, 6, 8};
+constexpr Policy kFwdBiasWeightPolicy = {32, 4, 4, 4, 8};
 // Forward outputs below this size (the Megatron ffn-4096 shape's 67 MB among
 // them) use 16-byte packs at 6 CTAs per SM: 29.4 us against 33.1 us on the
 // one-pass 32-byte grid; the Llama-like (235 MB) and large-FFN shapes are
@@ -134,10 +142,10 @@ constexpr int64_t kFwdSmallBytes = (int64_t)128 << 20;
 // Llama-like 165.3 against 168.0, large FFN 373 against 378 (256-thread CTAs
 // with one 32-byte pack: 54.3 / 176.2 / 394.8).  The bias and per-token-weight
 // forms stay at 16-byte packs (their tile and row kernels are built on them).
-constexpr Policy kBwdPolicy = {32, 0, 0, 6};
+constexpr Policy kBwdPolicy = {32, 0, 0, 0, 6};
 constexpr int kBwdModeMaxPack = 16;
 // The per-token-weighted backward is one CTA per row, persistent over rows.
-constexpr Policy kRowPolicy = {16, 3, 3, 6};
+constexpr Policy kRowPolicy = {16, 3, 3, 3, 6};
 // The bias tile kernel is launched as one wave of per_sm CTAs per SM, each
 // covering tile_cols columns of each half, with its registers held to
 // min_ctas CTAs per SM; the workspace size follows from it.  Packs of 8 and
@@ -183,7 +191,8 @@ constexpr BiasShape bias_shape(bool weighted, int pack_bytes) {
 
 // Resident CTAs per SM to launch with, 0 for a one-pass grid.
 constexpr int ctas_cap(const Policy &p, int pack_bytes) {
-    return pack_bytes >= 32 ? p.ctas_wide : (pack_bytes > 4 ? p.ctas_medium : p.ctas_narrow);
+    return pack_bytes >= 32 ? p.ctas_wide
+                             : pack_bytes >= 16 ? p.ctas_16 : pack_bytes >= 8 ? p.ctas_8 : p.ctas_narrow;
 }
 
 // Packs in flight per operand per thread: one 32-byte pack, two 16-byte
@@ -394,7 +403,8 @@ swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
     constexpr int U = unroll_for(E::kBytes * VEC);
     constexpr int cap = ctas_cap(MODE == swiglu::kPlain        ? kFwdPolicy
                                  : MODE == swiglu::kBiasWeight ? kFwdBiasWeightPolicy
-                                                               : kFwdModePolicy,
+                                 : MODE == swiglu::kBias       ? kFwdBiasPolicy
+                                                               : kFwdWeightPolicy,
                                  E::kBytes * VEC);
     // the one-pass grid runs 128-thread CTAs: 0.5-1.7 % faster than 256 on the
     // large-FFN and Llama-like shapes
