@@ -181,12 +181,18 @@ constexpr BiasShape kWeightedBiasNarrow = {1024, 4, 4};
 //   1024 x 4, no ring               0.815 / 0.714    0.768 / 0.722
 //   1024 x 4, 2-row ring            0.872 / 0.727    0.794 / 0.707
 // so bf16 takes the ring on the 2048-column shape, fp32 the 1024-column shape
-// (with the ring for the bias form only).
+// (with the ring for the bias form only).  bf16 on 4-byte packs (two elements)
+// also takes the ring on the 2048-column shape (bf16 [8192, 2 x 14334]: 0.708
+// -> 0.775 / 0.661 -> 0.703; the ring on the 1024-column shape: 0.711 /
+// 0.667).
+template <typename E>
+constexpr bool bias_narrow(int pack_bytes) {
+    return E::kBytes == 2 ? pack_bytes <= 2 : pack_bytes <= 8;
+}
 template <typename E>
 constexpr BiasShape bias_shape(bool weighted, int pack_bytes) {
-    return pack_bytes <= 4 || (pack_bytes == 8 && E::kBytes == 4)
-               ? (weighted ? kWeightedBiasNarrow : kBiasNarrow)
-               : (weighted ? kWeightedBiasWide : kBiasWide);
+    return bias_narrow<E>(pack_bytes) ? (weighted ? kWeightedBiasNarrow : kBiasNarrow)
+                                      : (weighted ? kWeightedBiasWide : kBiasWide);
 }
 
 // Resident CTAs per SM to launch with, 0 for a one-pass grid.
@@ -625,12 +631,16 @@ swiglu_status_t launch_bwd_weighted(const BwdArgs &a, cudaStream_t stream) {
 
 // Rows in flight through the bias tile kernel's cp.async ring (0: plain
 // register loads); see swiglu_bwd_bias_kernel.  16-byte packs: 2.  8-byte
-// packs: 2 but for fp32 with weights (see bias_shape).  4-byte packs and
-// narrower: none (fp32, odd n: a 2-row ring ran 139 us against 97 us without
-// on the odd-width workload's bias backward).
+// packs: 2 but for fp32 with weights (see bias_shape).  4-byte packs: 2 for
+// bf16 (two elements a pack), none for fp32 (one element; odd n: a 2-row ring
+// ran 139 us against 97 us without on the odd-width workload's bias
+// backward).  Narrower packs: none.
 template <typename E, bool WEIGHTED>
 constexpr int bias_stages(int pack_bytes) {
-    return pack_bytes == 16 ? 2 : (pack_bytes == 8 && !(E::kBytes == 4 && WEIGHTED) ? 2 : 0);
+    return pack_bytes == 16                                     ? 2
+           : pack_bytes == 8 && !(E::kBytes == 4 && WEIGHTED) ? 2
+           : pack_bytes == 4 && E::kBytes == 2                 ? 2
+                                                               : 0;
 }
 // Rows of dw partial sums the weights + bias tile kernel batches per barrier
 // (16 leaves room for the ring at 3 CTAs per SM; same speed as 32).
