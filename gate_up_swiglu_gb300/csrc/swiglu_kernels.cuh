@@ -1220,14 +1220,42 @@ __global__ void __launch_bounds__(kThreads, MINB) swiglu_bwd_bias_kernel(const B
     }
     if (STAGES > 0) cp_async_wait<0>();
     const int64_t n = (int64_t)p.nvec * VEC;
+    // The column sums go out as whole vectors: a thread's VEC sums per half
+    // are consecutive, and one scalar store per sum left each warp store
+    // touching 32 separate sectors (ffn-4096 weights + bias backward: 0.789
+    // -> 0.847 of the copy rate with the vector stores, bias 0.882 -> 0.899).
+    // The workspace is 16-byte aligned (32-byte stores when it is 32-byte
+    // aligned), and n is a multiple of VEC, so every vector below is aligned.
     float *part = p.partial + group * 2 * n;
+    const bool part32 = (reinterpret_cast<uintptr_t>(p.partial) & 31) == 0;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
         if (c[k] < p.nvec) {
+            float *pg = part + (int64_t)c[k] * VEC, *pu = pg + n;
+            if (VEC == 8 && part32) {
+                uint32_t wg[8], wu[8];
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) {
-                part[(int64_t)c[k] * VEC + i] = ag[k][i];
-                part[n + (int64_t)c[k] * VEC + i] = au[k][i];
+                for (int i = 0; i < 8; ++i) {
+                    wg[i] = __float_as_uint(ag[k][i % VEC]);
+                    wu[i] = __float_as_uint(au[k][i % VEC]);
+                }
+                St<32, kStPlain>::run(pg, wg);
+                St<32, kStPlain>::run(pu, wu);
+            } else if constexpr (VEC % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < VEC; i += 4) {
+                    *reinterpret_cast<float4 *>(pg + i) = make_float4(ag[k][i], ag[k][i + 1], ag[k][i + 2], ag[k][i + 3]);
+                    *reinterpret_cast<float4 *>(pu + i) = make_float4(au[k][i], au[k][i + 1], au[k][i + 2], au[k][i + 3]);
+                }
+            } else if constexpr (VEC == 2) {
+                *reinterpret_cast<float2 *>(pg) = make_float2(ag[k][0], ag[k][1]);
+                *reinterpret_cast<float2 *>(pu) = make_float2(au[k][0], au[k][1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    pg[i] = ag[k][i];
+                    pu[i] = au[k][i];
+                }
             }
         }
     }
