@@ -773,7 +773,15 @@ swiglu_status_t dispatch_bwd(const BwdArgs &a, cudaStream_t st) {
     return launch_bwd<E, 1, IP>(a, st);
 }
 
+// The kernels load and store whole elements, so every pointer must sit on a
+// multiple of its element size.
+bool on_element(const void *p, int bytes) { return (uintptr_t)p % (uintptr_t)bytes == 0; }
+
 swiglu_status_t run_fwd(swiglu_dtype_t dtype, const FwdArgs &a, swiglu_stream_t stream) {
+    const int eb = dtype == SWIGLU_F32 ? 4 : 2;
+    if (!on_element(a.g.p, eb) || !on_element(a.u.p, eb) || !on_element(a.y.p, eb) ||
+        !on_element(a.bias_g, eb) || !on_element(a.bias_u, eb) || !on_element(a.w, 4))
+        return SWIGLU_ERR_STRIDE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWIGLU_F32) return dispatch_fwd<swiglu::F32>(a, s);
     return dispatch_fwd<swiglu::BF16>(a, s);
@@ -781,6 +789,12 @@ swiglu_status_t run_fwd(swiglu_dtype_t dtype, const FwdArgs &a, swiglu_stream_t 
 
 swiglu_status_t run_bwd(swiglu_dtype_t dtype, bool in_place, const BwdArgs &a,
                         swiglu_stream_t stream) {
+    const int eb = dtype == SWIGLU_F32 ? 4 : 2;
+    if (!on_element(a.dy.p, eb) || !on_element(a.g.p, eb) || !on_element(a.u.p, eb) ||
+        !on_element(a.dg.p, eb) || !on_element(a.du.p, eb) || !on_element(a.bias_g, eb) ||
+        !on_element(a.bias_u, eb) || !on_element(a.dbias, eb) || !on_element(a.w, 4) ||
+        !on_element(a.dw, 4))
+        return SWIGLU_ERR_STRIDE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == SWIGLU_F32)
         return in_place ? dispatch_bwd<swiglu::F32, true>(a, s) : dispatch_bwd<swiglu::F32, false>(a, s);

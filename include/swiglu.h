@@ -28,6 +28,9 @@
  *     swiglu_gateup_bias_bwd_noalloc (below), part of the loaded module.
  *   - Sizes and row strides are counted in ELEMENTS of the dtype; within a row
  *     elements are contiguous.  Row r of x starts at x + r * x_row_stride.
+ *   - Every pointer is aligned to its element size: 2 bytes for bf16, 4 for
+ *     fp32 and for the fp32 per-token weights and their gradient (else
+ *     SWIGLU_ERR_STRIDE, before anything is launched).
  *   - All tensors of one call share one dtype.  Arithmetic is fp32; each result
  *     is rounded once to the dtype (round to nearest even).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and runs
@@ -69,7 +72,8 @@ typedef enum {
     SWIGLU_ERR_DTYPE = -2,  /* dtype is not a swiglu_dtype_t value              */
     SWIGLU_ERR_SHAPE = -3,  /* rows or n negative, or n > SWIGLU_MAX_N, or the
                                byte extent of a tensor overflows int64          */
-    SWIGLU_ERR_STRIDE = -4, /* a row stride is shorter than its row             */
+    SWIGLU_ERR_STRIDE = -4, /* a row stride is shorter than its row, or a
+                               pointer is not aligned to its element size      */
     SWIGLU_ERR_ALIAS = -5,  /* an output overlaps an input it must not overlap  */
     SWIGLU_ERR_CUDA = -6,   /* the CUDA runtime reported an error; see
                                swiglu_last_cuda_error()                         */

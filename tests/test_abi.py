@@ -119,6 +119,19 @@ def test_bwd_rejections(sw):
     assert bwd(sw, ip=1, dx=X, dy=X + 16) == -5
 
 
+def test_pointers_must_sit_on_elements(sw):
+    """A pointer off its element size is refused before anything is launched
+    (the kernels load and store whole elements)."""
+    assert fwd(sw, x=X + 1) == -4
+    assert fwd(sw, y=Y + 1) == -4
+    assert fwd(sw, x=X + 2, dt=F32) == -4
+    assert fwd(sw, y=Y + 6, dt=F32) == -4
+    assert bwd(sw, dy=DY + 1) == -4
+    assert bwd(sw, dx=DX + 3) == -4
+    assert bwd(sw, x=X + 2, dt=F32) == -4
+    assert bwd(sw, ip=1, dx=X + 1, x=X + 1) == -4
+
+
 A, B, C, DA, DB = X, Y, DY, DX, 0x50_0000_0000
 
 

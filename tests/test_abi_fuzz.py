@@ -50,6 +50,8 @@ def expect_fwd(x, y, rows, n, sx, sy, dt):
     eb = 4 if dt == 0 else 2
     if overl(span(x, rows, 2 * n, sx, eb), span(y, rows, n, sy, eb)):
         return ALIAS
+    if x % eb or y % eb:  # every pointer on its element size
+        return STRIDE
     return CUDA
 
 
@@ -78,6 +80,8 @@ def expect_bwd(dy, x, dx, rows, n, sdy, sx, sdx, dt, ip):
             return ALIAS
     elif overl(s_dx, s_x) or overl(s_dx, s_dy):
         return ALIAS
+    if dy % eb or x % eb or dx % eb:  # every pointer on its element size
+        return STRIDE
     return CUDA
 
 
