@@ -153,7 +153,7 @@ constexpr Policy kRowPolicy = {16, 3, 3, 3, 6};
 // SM on the large-FFN and Llama-like shapes, the bias form did best at 2
 // (407.6 / 189.0 us against 424.7 / 196.7 us for the ring-less kernel at 3),
 // the weights + bias form at 3 (429.0 / 202.7 us against 475.2 / 221.1; 466 /
-// 215 at 2).  Packs of 4 bytes and less (one element each, no ring): with
+// 215 at 2).  Single-element packs (fp32 4 bytes, bf16 2 bytes; no ring): with
 // that shape the kernel waits on its loads (2 CTAs per SM: 23 % of the warps
 // active, issue 46 %, fp32 odd-width bias form), and at 4 CTAs per SM its 2048
 // columns spill.  1024-column tiles at 4 CTAs per SM (53-63 registers) did
@@ -185,6 +185,7 @@ constexpr BiasShape kWeightedBiasNarrow = {1024, 4, 4};
 // also takes the ring on the 2048-column shape (bf16 [8192, 2 x 14334]: 0.708
 // -> 0.775 / 0.661 -> 0.703; the ring on the 1024-column shape: 0.711 /
 // 0.667).
+// The 1024-column shape: single-element packs, and fp32 pairs (8 bytes).
 template <typename E>
 constexpr bool bias_narrow(int pack_bytes) {
     return E::kBytes == 2 ? pack_bytes <= 2 : pack_bytes <= 8;
