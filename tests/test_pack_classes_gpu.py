@@ -11,7 +11,8 @@ The widths follow from n and the storage type (fresh, aligned buffers):
   bf16 n = 4096                 16-byte packs (the reference point)
 Every output is compared with the oracle element by element at the
 tolerances of tests/helpers.py; the reductions (dbias, dw) against the
-summation bound of the bias tests.
+summation bound of the bias tests; and every in-place backward must give the
+out-of-place bits.
 """
 import pytest
 import torch
@@ -93,3 +94,16 @@ def test_pack_class_every_form(sw, dt, n):
     t = dy64 * oracle.bias_fwd(x64, b64)
     assert_reduction(dww, t.sum(1), t.abs().sum(1), _wb_dw_depth(n), f"{what} weighted bias dw", elem=dt,
                      count=n)
+
+    # the in-place forms (coherent loads, dx over x) give the out-of-place bits
+    for name, call, ref in (
+            ("weighted", lambda xi: sw.swiglu_gateup_weighted_bwd(dy, xi, w, in_place=True), (dxw, dw)),
+            ("bias", lambda xi: sw.swiglu_gateup_bias_bwd(dy, xi, bias, in_place=True), (dxb, db)),
+            ("weighted bias", lambda xi: sw.swiglu_gateup_weighted_bias_bwd(dy, xi, bias, w, in_place=True),
+             (dxwb, dbw, dww))):
+        xi = x.clone()
+        got = call(xi)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), f"{what}: in-place {name} backward differs from out of place"
+        assert torch.equal(xi, ref[0]), f"{what}: in-place {name} dx not written over x"
