@@ -290,6 +290,24 @@ def test_weighted_full_size_rows(sw):
                      elem=x.dtype, count=w_.n)
 
 
+@pytest.mark.parametrize("rows", [1, 3, 305])
+def test_weighted_long_rows_odd_counts(sw, rows):
+    """The per-token-weighted kernel takes two rows per pass; rows longer than
+    2048 16-byte packs run its unbounded form.  Odd row counts leave a last
+    pass with one row.  dx elementwise, dw against the exact row sums."""
+    n = 20480  # 2560 packs of 8 bf16
+    g = torch.Generator().manual_seed(rows)
+    x_c = (torch.randn(rows, 2 * n, generator=g) * 3).to(torch.bfloat16)
+    dy_c = torch.randn(rows, n, generator=g).to(torch.bfloat16)
+    w_c = torch.rand(rows, generator=g)
+    dx, dw = sw.swiglu_gateup_weighted_bwd(dy_c.cuda(), x_c.cuda(), w_c.cuda())
+    torch.cuda.synchronize()
+    assert_parity(dx, oracle.weighted_bwd(dy_c, x_c, w_c)[0], f"long rows {rows}: weighted dx")
+    t = dy_c.double() * oracle.fwd(x_c.double())
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, f"long rows {rows}: weighted dw",
+                     elem=torch.bfloat16, count=n)
+
+
 def test_empty_and_workspace_errors(sw):
     n = 64
     bias = torch.randn(2 * n, device="cuda")
