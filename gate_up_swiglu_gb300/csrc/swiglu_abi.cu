@@ -128,7 +128,11 @@ constexpr Policy kFwdPolicy = {32, 0, 6, 0, 8};
 // against 258.0 / 254.3 us at 4 CTAs per SM; Llama-like 101.4 / 100.2 against
 // 109.5 / 108.9).  Both together: persistent at 4 CTAs per SM (234.8 us
 // against 249.9 on one pass of 256-thread CTAs and 325.8 of 128-thread ones).
-constexpr Policy kFwdBiasPolicy = {32, 0, 4, 4, 8};
+// The bias forward on 8-byte packs: 8 CTAs per SM with two packs in flight
+// (bf16 [8192, 2 x 14340] 0.817 -> 0.848 of the copy rate, fp32 [8192, 2 x
+// 4098] 0.842 -> 0.851, against 4 CTAs with four packs; with both the weights
+// + bias forward fell from 0.82 to 0.74 and keeps 4 with four).
+constexpr Policy kFwdBiasPolicy = {32, 0, 4, 8, 8};
 constexpr Policy kFwdWeightPolicy = {32, 0, 4, 6, 8};
 constexpr Policy kFwdBiasWeightPolicy = {32, 4, 4, 4, 8};
 // Forward outputs below this size (the Megatron ffn-4096 shape's 67 MB among
@@ -407,7 +411,7 @@ bool bias_workspace(int64_t rows, int64_t n, int sms, bool weighted, size_t &dw_
 
 template <typename E, int VEC, int MODE>
 swiglu_status_t launch_fwd(const FwdArgs &a, cudaStream_t stream) {
-    constexpr int U = unroll_for(E::kBytes * VEC);
+    constexpr int U = MODE == swiglu::kBias && E::kBytes * VEC == 8 ? 2 : unroll_for(E::kBytes * VEC);
     constexpr int cap = ctas_cap(MODE == swiglu::kPlain        ? kFwdPolicy
                                  : MODE == swiglu::kBiasWeight ? kFwdBiasWeightPolicy
                                  : MODE == swiglu::kBias       ? kFwdBiasPolicy
