@@ -308,12 +308,13 @@ def test_weighted_long_rows_odd_counts(sw, rows):
                      elem=torch.bfloat16, count=n)
 
 
-def test_bias_forms_megatron_full_every_element(sw):
-    """The ffn-4096 Megatron workload at full size (8192 rows), in the launch
-    configuration the bench times: every element of y and dx of the bias,
-    weighted and weights + bias forms against the oracle, and every dbias
-    column and dw row against the exact sums."""
-    w_ = W.WORKLOADS["megatron_4096_bf16"]
+@pytest.mark.parametrize("name", ["megatron_4096_bf16", "llama_14336_bf16_2d"])
+def test_bias_forms_full_every_element(sw, name):
+    """The ffn-4096 Megatron and the Llama-like workloads at full size (8192
+    rows), in the launch configuration the bench times: every element of y and
+    dx of the bias, weighted and weights + bias forms against the oracle, and
+    every dbias column and dw row against the exact sums."""
+    w_ = W.WORKLOADS[name]
     x_c, dy_c = W.make_inputs(w_, "cpu")
     x_c, dy_c = x_c.reshape(-1, 2 * w_.n), dy_c.reshape(-1, w_.n)
     rows, n = x_c.shape[0], w_.n
@@ -323,22 +324,22 @@ def test_bias_forms_megatron_full_every_element(sw):
     x, dy, bias, wts = x_c.cuda(), dy_c.cuda(), b_c.cuda(), w_c.cuda()
     x64, dy64, b64 = x_c.double(), dy_c.double(), b_c.double()
 
-    assert_parity(sw.swiglu_gateup_bias_fwd(x, bias), oracle.bias_fwd(x_c, b_c), "megatron bias fwd")
+    assert_parity(sw.swiglu_gateup_bias_fwd(x, bias), oracle.bias_fwd(x_c, b_c), f"{name} bias fwd")
     dx, db = sw.swiglu_gateup_bias_bwd(dy, x, bias)
-    assert_parity(dx, oracle.bias_bwd(dy_c, x_c, b_c)[0], "megatron bias dx")
+    assert_parity(dx, oracle.bias_bwd(dy_c, x_c, b_c)[0], f"{name} bias dx")
     dx64, db64 = oracle.bias_bwd(dy64, x64, b64)
-    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), "megatron dbias",
+    assert_reduction(db, db64, dx64.abs().sum(0), _bias_depth(rows, n), f"{name} dbias",
                      elem=torch.bfloat16, count=rows)
 
-    assert_parity(sw.swiglu_gateup_weighted_fwd(x, wts), oracle.weighted_fwd(x_c, w_c), "megatron weighted fwd")
+    assert_parity(sw.swiglu_gateup_weighted_fwd(x, wts), oracle.weighted_fwd(x_c, w_c), f"{name} weighted fwd")
     dx, dw = sw.swiglu_gateup_weighted_bwd(dy, x, wts)
-    assert_parity(dx, oracle.weighted_bwd(dy_c, x_c, w_c)[0], "megatron weighted dx")
+    assert_parity(dx, oracle.weighted_bwd(dy_c, x_c, w_c)[0], f"{name} weighted dx")
     t = dy64 * oracle.fwd(x64)
-    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, "megatron weighted dw",
+    assert_reduction(dw, t.sum(1), t.abs().sum(1), n / 256 + 13, f"{name} weighted dw",
                      elem=torch.bfloat16, count=n)
 
     _check_weighted_bias(dy_c, x_c, b_c, w_c, sw.swiglu_gateup_weighted_bias_fwd(x, bias, wts),
-                         *sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts), "megatron weighted bias")
+                         *sw.swiglu_gateup_weighted_bias_bwd(dy, x, bias, wts), f"{name} weighted bias")
 
 
 def test_empty_and_workspace_errors(sw):
